@@ -1,0 +1,384 @@
+"""Benchmark of the MoE expert layer on GB300 through libmoe's C-ABI.
+
+One step = one moe_forward (plan -> quant/scatter -> GEMM1+act -> GEMM2 ->
+combine) over one batch of synthetic tokens already resident in HBM.  Default
+workload: the BF16 contiguous prefill (T=4096, K=2048, I=768, 128 experts,
+top-8).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 (launched by torch.distributed.run, one rank per GPU) runs N
+independent replicas: the layer has no cross-GPU step on one node's expert
+set, so every rank processes its own batch; timing is the max over ranks.
+"--impl reference" times the CPU oracle (fp64, numpy) on the host cores on a
+bounded sample of the same workload.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_layer_ep_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s, grouped-GEMM TFLOPS & % of roofline on 1xGB300"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_prefill", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--T", type=int, default=None, help="override the token count")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload(args):
+    w = dict(synth.WORKLOADS[args.workload])
+    if args.T:
+        w["T"] = args.T
+    return w
+
+
+def build_inputs(w, device):
+    T, K, I = w["T"], w["K"], w["I"]
+    x = synth.activations(T, K, w["seed"], device)
+    ids, wts = synth.routing(T, w["E_global"], w["topk"], w["seed"] + 1, w["zipf_s"])
+    es = w["expert_start"]
+    if w["dtype"] == "fp8":
+        w13, w13s = synth.fp8_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
+        w2, w2s = synth.fp8_expert_weights(w["E_local"], K, I, w["seed"] + 3, device, es)
+    else:
+        w13 = synth.bf16_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
+        w2 = synth.bf16_expert_weights(w["E_local"], K, I, w["seed"] + 3, device, es)
+        w13s = w2s = None
+    return x, ids, wts, (w13, w13s, w2, w2s)
+
+
+def work_model(w, ids):
+    """Algorithmic work of one step (valid rows only)."""
+    T, K, I, E_l, es = w["T"], w["K"], w["I"], w["E_local"], w["expert_start"]
+    ids = ids.numpy()
+    loc = (ids >= es) & (ids < es + E_l)
+    A = int(loc.sum())
+    nonempty = len(np.unique(ids[loc]))
+    esz = 1 if w["dtype"] == "fp8" else 2
+    flops1 = 2.0 * A * K * 2 * I
+    flops2 = 2.0 * A * I * K
+    w13_bytes = nonempty * 2 * I * K * esz
+    w2_bytes = nonempty * K * I * esz
+    # GEMM1 reads its weights, the valid a rows, writes h; GEMM2 likewise.
+    g1_bytes = w13_bytes + A * K * esz + A * I * esz
+    g2_bytes = w2_bytes + A * I * esz + A * K * 2
+    return {"A": A, "nonempty": nonempty, "flops1": flops1, "flops2": flops2, "g1_bytes": g1_bytes,
+            "g2_bytes": g2_bytes, "weights_bytes": w13_bytes + w2_bytes,
+            "layer_bytes": w13_bytes + w2_bytes + T * K * 2 * 2 + 2 * A * K * esz + 2 * A * I * esz + 2 * A * K * 2}
+
+
+class OracleRunner:
+    """The fp64 oracle, as it stands, on a sample of the workload's tokens.
+    Expert weights are dequantised once, outside any timed region."""
+
+    def __init__(self, w, x, ids, wts, weights):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.x64 = x.float().cpu().numpy().astype(np.float64)
+        self.ids = ids.cpu().numpy()
+        self.wts = wts.cpu().numpy()
+        self.weights = tuple(t.cpu() if t is not None else None for t in weights)
+        self.cache = {}
+
+    def expert(self, e):
+        if e not in self.cache:
+            w13, w13s, w2, w2s = self.weights
+            if self.w["dtype"] == "fp8":
+                a = self.oracle.dequant_fp8_weights(w13[e:e + 1].numpy(), w13s[e:e + 1].numpy().astype(np.int64) - 127)[0]
+                b = self.oracle.dequant_fp8_weights(w2[e:e + 1].numpy(), w2s[e:e + 1].numpy().astype(np.int64) - 127)[0]
+            else:
+                a = w13[e].float().numpy().astype(np.float64)
+                b = w2[e].float().numpy().astype(np.float64)
+            self.cache[e] = (a, b)
+        return self.cache[e]
+
+    def run(self, seconds_target):
+        w = self.w
+        T, K, I = w["T"], w["K"], w["I"]
+        es, El = w["expert_start"], w["E_local"]
+        n, elapsed, chunk = 0, 0.0, 8
+        while n < T and elapsed < seconds_target:
+            sl = slice(n, min(T, n + chunk))
+            loc = sorted({int(i) - es for i in self.ids[sl].reshape(-1) if es <= int(i) < es + El})
+            w13d = np.stack([self.expert(e)[0] for e in loc]) if loc else np.zeros((0, 2 * I, K))
+            w2d = np.stack([self.expert(e)[1] for e in loc]) if loc else np.zeros((0, K, I))
+            remap = np.array([[loc.index(int(i) - es) if es <= int(i) < es + El else -1 for i in row]
+                              for row in self.ids[sl]])
+            t0 = time.perf_counter()
+            self.oracle.forward_layout(self.x64[sl], w13d, w2d, remap, self.wts[sl], w["dtype"],
+                                       E_global=max(1, len(loc)), layout="compact")
+            elapsed += time.perf_counter() - t0
+            n = sl.stop
+        return {"value": n / elapsed, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"first {n} of {T} tokens of workload {w['name']}, fp64 numpy oracle (layout path), "
+                          f"{elapsed:.1f} s", "tokens": n}
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    x, ids, wts, weights = build_inputs(w, "cpu")
+    runner = OracleRunner(w, x, ids, wts, weights)
+    per_step = []
+    for s in range(args.warmup + args.steps):
+        r = runner.run(seconds_target=2.0)
+        if s >= args.warmup:
+            per_step.append(r)
+    value = statistics.median(r["value"] for r in per_step)
+    n_tok = per_step[0]["tokens"]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * n_tok / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w["name"], "T": w["T"], "K": w["K"], "I": w["I"],
+                                            "E": w["E_local"], "topk": w["topk"]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": per_step[0]["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, world, rank, local):
+    import moe_expert_layer_ep_gb300 as M
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x, ids_host, w_host, weights = build_inputs(w, dev)
+    ids, wts = ids_host.to(dev), w_host.to(dev)
+    shape = M.make_shape(w["T"], w["K"], w["I"], w["E_global"], w["E_local"], w["topk"], w["dtype"], w["layout"],
+                         w["expert_start"], w.get("max_m", 0) or (w["T"] if w["layout"] == "masked" else 0))
+    ctx = M.moe_ctx_create(shape, *weights)
+    ws = M.alloc_workspace(ctx, dev)
+    out = torch.empty((w["T"], w["K"]), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    M.moe_clear_device_status(ws)
+
+    stages = [lambda: M.moe_plan_layout(ctx, ids, ws),
+              lambda: M.moe_quant_scatter(ctx, x, ws),
+              lambda: M.moe_grouped_gemm_w13_act(ctx, ws),
+              lambda: M.moe_grouped_gemm_w2(ctx, ws),
+              lambda: M.moe_combine(ctx, wts, ws, out)]
+    for _ in range(args.warmup):
+        M.moe_forward(ctx, x, ids, wts, ws, out)
+    torch.cuda.synchronize()
+    status = M.moe_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {M.STATUS_NAMES.get(status, status)} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            for i, fn in enumerate(stages):
+                fn()
+                ev[s][i + 1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    stage_ms = np.array([[ev[s][i].elapsed_time(ev[s][i + 1]) for i in range(len(stages))]
+                         for s in range(args.steps)])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the C-ABI with host buffers: h2d of x / ids / weights,
+    # forward, d2h of out, every step
+    x_h = x.cpu().pin_memory()
+    ids_h = ids.cpu().pin_memory()
+    w_h = wts.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    for _ in range(2):
+        x.copy_(x_h, non_blocking=True); ids.copy_(ids_h, non_blocking=True); wts.copy_(w_h, non_blocking=True)
+        M.moe_forward(ctx, x, ids, wts, ws, out)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_h, non_blocking=True); ids.copy_(ids_h, non_blocking=True); wts.copy_(w_h, non_blocking=True)
+        M.moe_forward(ctx, x, ids, wts, ws, out)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert M.moe_read_device_status(ws) == 0
+
+    if rank != 0:
+        return
+    peaks = load_peaks()
+    wm = work_model(w, ids_host)
+    T = w["T"]
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1000.0)
+    med = np.median(stage_ms, axis=0)
+    g1_ms, g2_ms = float(med[2]), float(med[3])
+    gemm_tflops = (wm["flops1"] + wm["flops2"]) / ((g1_ms + g2_ms) / 1000.0) / 1e12
+    fp8 = w["dtype"] == "fp8"
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    g1_gbs = wm["g1_bytes"] / (g1_ms / 1000.0) / 1e9
+    g1_tf = wm["flops1"] / (g1_ms / 1000.0) / 1e12
+    # dominant kernel: GEMM1; bound = whichever of its roofline times is larger
+    t_hbm = wm["g1_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = wm["flops1"] / (tensor_peak * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": round(g1_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(g1_gbs / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(g1_tf, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": round(g1_tf / tensor_peak, 4)}
+    roof.update({"kernel": "grouped_gemm_kernel<stage 1>", "traffic": None,
+                 "peak_source": peaks["source"] + (" (bf16 x 2 for fp8)" if fp8 else "")})
+    layer_roof_ms = 1000.0 * max(wm["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                                 (wm["flops1"] + wm["flops2"]) / (tensor_peak * 1e12))
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3/ue8m0" if fp8 else "bf16",
+        "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": w["name"], "T": T, "K": w["K"], "I": w["I"], "E": w["E_local"],
+                   "topk": w["topk"], "layout": w["layout"], "l2": "weights larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}"},
+        "gemm_tflops": round(gemm_tflops, 1),
+        "layer_roofline_frac": round(layer_roof_ms / ms_per_step, 4),
+        "stage_ms": {n: round(float(v), 4) for n, v in zip(["plan", "quant_scatter", "gemm_w13_act", "gemm_w2",
+                                                            "combine"], med)},
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "e2e": {"value": round(world * T * args.steps / (e2e_ms / 1000.0), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * 2 + ids.numel() * 4 + wts.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2},
+        "gpu_launches": M.moe_forward_launches(ctx) * args.steps,
+        "work": {"assignments": wm["A"], "nonempty_experts": wm["nonempty"],
+                 "padded_rows": int(M.ws_view(ctx, ws, "meta")[0].item())},
+    }
+    if not args.no_cpu_baseline:
+        cb = OracleRunner(w, x, ids_host, w_host, weights).run(seconds_target=12.0)
+        cb.pop("tokens")
+        line["cpu_baseline"] = cb
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    w = workload(args)
+    w["name"] = args.workload
+    if world > 1:
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, world, rank)
+        else:
+            run_ours(args, w, world, rank, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

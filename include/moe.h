@@ -1,0 +1,211 @@
+/*
+ * libmoe -- single-GPU MoE expert layer for GB300 (sm_103a).
+ *
+ * The layer, as described by three sglang PR reports:
+ *   [P1] "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report)
+ *   [P2] "Add BF16 support to EP-MoE for DeepGEMM"    (sglang PR #17392 report)
+ *   [P3] "[Feature] Support BF16 and batch-invariant inference with DeepEP v2"
+ *        (sglang PR #38160 report)
+ *
+ *   plan_layout      top-k routing -> per-expert row layout      [P1 "实现拆解" 2-3]
+ *   quant_scatter    x -> FP8 1x128 UE8M0 (or BF16) expert rows   [P1 "实现拆解" 3, P2 step 3]
+ *   grouped_gemm_w13_act   h = silu(a W1^T) * (a W3^T)            [P2 "关键源码片段" deep_gemm.py]
+ *   grouped_gemm_w2        y = h W2^T                             [P2 same]
+ *   combine          out[t] = sum_j w[t,j] * y[src2dst[t,j]]      [P1 "风险与影响" 2, P3 "实现拆解" 3]
+ *   forward          all five, in order, on one stream
+ *
+ * Conventions for every call below
+ * --------------------------------
+ * - Pointers named "device" are CUDA device pointers; all of them must be
+ *   16-byte aligned.  The caller allocates and owns every buffer (weights,
+ *   inputs, outputs, workspace); the library allocates no device memory and
+ *   frees nothing of the caller's.
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   The hot calls only enqueue work: no host synchronisation, no allocation,
+ *   static shapes, so a sequence of them can be captured in a CUDA graph.
+ * - Errors the host can see (bad pointers, sizes, unsupported shapes) are
+ *   returned before anything is launched.  Errors in the data (an expert id
+ *   outside [-1, E_global), a masked expert with more than max_m rows, a wait
+ *   that timed out inside a kernel) set a sticky status word in the
+ *   workspace; the offending item is skipped and the call still returns
+ *   MOE_OK.  Read the word with moe_read_device_status().
+ * - Sizes are int64; the weights of the large shapes exceed 2^31 elements.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,      /* null / misshaped argument */
+  MOE_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. K % 128 != 0) */
+  MOE_ERR_BUFFER_TOO_SMALL = 3, /* reserved */
+  MOE_ERR_MISALIGNED = 4,       /* a pointer is not 16-byte aligned */
+  MOE_ERR_CUDA = 5,             /* a CUDA runtime / driver call failed */
+  MOE_ERR_EXPERT_ID = 6,        /* device: topk id outside [-1, E_global) */
+  MOE_ERR_MASKED_OVERFLOW = 7,  /* device: masked expert got more than max_m rows */
+  MOE_ERR_TIMEOUT = 8,          /* device: a bounded wait inside a kernel ran out */
+  MOE_ERR_DTYPE_MISMATCH = 9    /* weight arguments contradict the declared dtype */
+} moe_status_t;
+
+/* Arithmetic of the expert GEMMs [P1 "实现拆解" 1 and 3; P2 "实现拆解" 2]. */
+typedef enum {
+  MOE_DTYPE_FP8_E4M3_UE8M0 = 0, /* FP8 e4m3 operands, UE8M0 scales: 1x128 (activations), 128x128 (weights) */
+  MOE_DTYPE_BF16 = 1            /* bf16 operands, no scales */
+} moe_dtype_t;
+
+/* Row layout of the expert inputs [P1 "实现拆解" 2, "关键源码片段" deep_gemm.py]. */
+typedef enum {
+  MOE_LAYOUT_AUTO = 0,    /* masked iff E_global > E_local && E_local <= 32, else compact */
+  MOE_LAYOUT_COMPACT = 1, /* [all_tokens, K], experts padded to block_e rows, m_indices row->expert */
+  MOE_LAYOUT_MASKED = 2   /* [E_local, max_m, K] with masked_m[E_local] valid rows per expert */
+} moe_layout_t;
+
+/* Static shape of one layer call (MoeRunnerConfig fields [P1 "关键源码片段"
+ * deep_gemm.py; P3 "关键源码片段" layer.py] plus the local expert range of
+ * [P3 "实现拆解" 1]). */
+typedef struct {
+  int64_t T;            /* tokens (>= 0) */
+  int64_t K;            /* hidden size, multiple of 128 */
+  int64_t I;            /* per-expert intermediate size, multiple of 128 */
+  int32_t E_global;     /* experts the router chooses from */
+  int32_t E_local;      /* experts held here, 1..1024 */
+  int32_t expert_start; /* first local expert; E_local + expert_start <= E_global */
+  int32_t topk;         /* experts per token, 1..64 */
+  int32_t block_e;      /* compact padding granularity; must be 128 */
+  int32_t dtype;        /* moe_dtype_t */
+  int32_t layout;       /* moe_layout_t */
+  int32_t reserved;
+  int64_t max_m;        /* masked layout: rows per expert (>= T); ignored for compact */
+} moe_shape_t;
+
+/* Byte offsets of the intermediates inside the caller's workspace (all
+ * 1024-byte aligned).  Rows of a/h/y: compact -> all_tokens; masked ->
+ * E_local * max_m (expert e's rows start at e * max_m). */
+typedef struct {
+  uint64_t total_bytes;
+  uint64_t status;      /* int32[4]: [0] = first moe_status_t seen on the device */
+  uint64_t meta;        /* int32[8]: [0] padded rows, [1] valid 128-row blocks */
+  uint64_t counts;      /* int32[E_local] assignments per local expert */
+  uint64_t padded;      /* int32[E_local] compact: counts rounded up to 128 */
+  uint64_t start;       /* int32[E_local] compact: first row of each expert */
+  uint64_t masked_m;    /* int32[E_local] masked: valid rows per expert */
+  uint64_t m_indices;   /* int32[all_tokens] compact: local expert per row, -1 = no token */
+  uint64_t src2dst;     /* int32[T * topk] destination row per assignment, -1 = dropped */
+  uint64_t block_info;  /* int32[4 * blocks]: {expert, first row, tma row, valid rows} */
+  uint64_t chunk_hist;  /* int32[chunks * E_local] plan scratch */
+  uint64_t chunk_rank;  /* int32[T * topk]         plan scratch */
+  uint64_t a;           /* [rows, K]  fp8 bytes or bf16: expert inputs */
+  uint64_t a_sf;        /* fp8: scale chunks of a (see moe_sf_offset) */
+  uint64_t h;           /* [rows, I]  fp8 bytes or bf16: silu(gate) * up */
+  uint64_t h_sf;        /* fp8: scale chunks of h */
+  uint64_t y;           /* [rows, K]  bf16: expert outputs */
+  int64_t rows;         /* rows of a / h / y */
+  int64_t all_tokens;   /* compact static bound (0 for masked) */
+  int64_t blocks;       /* static number of 128-row blocks */
+  int32_t layout;       /* resolved moe_layout_t */
+  int32_t chunks;       /* plan chunks of 256 assignments */
+} moe_ws_layout_t;
+
+typedef struct moe_ctx moe_ctx;
+
+/* Static compact row bound of [P1 "关键源码片段" deep_gemm.py]:
+ * block_e * (min(A, E) + (A - min(A, E)) / block_e).  Returns -1 on negative
+ * input or block_e <= 0. */
+int64_t moe_compact_all_tokens(int64_t num_assignments, int32_t num_experts, int32_t block_e);
+
+/* Layout choice of [P1 "关键源码片段" deep_gemm.py]: MOE_LAYOUT_MASKED iff
+ * E_global > E_local and E_local <= 32, else MOE_LAYOUT_COMPACT. */
+int32_t moe_choose_layout(int32_t E_global, int32_t E_local);
+
+/* Create a context for one layer shape and its weights (device pointers):
+ *   FP8:  w13 uint8 [E_local, 2I, K] e4m3, w13_sf uint8 [E_local, 2I/128, K/128] UE8M0,
+ *         w2  uint8 [E_local, K, I]  e4m3, w2_sf  uint8 [E_local, K/128, I/128]  UE8M0
+ *   BF16: w13 bf16 [E_local, 2I, K], w2 bf16 [E_local, K, I]; w13_sf = w2_sf = NULL
+ * Rows 0..I-1 of w13[e] are the gate projection W1, rows I..2I-1 the up
+ * projection W3 [P2 "关键源码片段" deep_gemm.py: the activation splits the
+ * GEMM output in halves].  Weights are read, never written, and must stay
+ * alive while the context is used.  A scale pointer given for BF16 or missing
+ * for FP8 is MOE_ERR_DTYPE_MISMATCH.  Host-only: builds the weight TMA
+ * descriptors; allocates no device memory. */
+moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uint8_t* w13_sf,
+                            const void* w2, const uint8_t* w2_sf, moe_ctx** out);
+void moe_ctx_destroy(moe_ctx* ctx);
+
+/* Workspace the caller must provide to the hot calls (device, 1024-byte
+ * aligned, at least total_bytes).  No initialisation is needed. */
+moe_status_t moe_workspace_layout(const moe_ctx* ctx, moe_ws_layout_t* out);
+moe_status_t moe_workspace_size(const moe_ctx* ctx, size_t* bytes);
+
+/* Step 1 [P1 "实现拆解" 2-3, "关键源码片段" ep_moe_kernels.py; P3 "实现拆解" 1]:
+ * topk_ids int32 [T, topk] (device; -1 = no assignment).  Writes counts,
+ * padded/start/m_indices (compact) or masked_m (masked), src2dst and the
+ * 128-row block table into ws.  Inside an expert, assignments keep their
+ * flattened t * topk + j order; rows without a token have m_indices -1. */
+moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, void* stream);
+
+/* Step 2 [P1 "实现拆解" 3; P2 "实现拆解" 3]: x bf16 [T, K] (device).  FP8:
+ * each 128-column group of a token gets the smallest power-of-two scale 2^s
+ * with amax <= 448 * 2^s (s clamped to [-127, 127]; byte s + 127) and every
+ * element is rounded to e4m3 (nearest-even, saturating) after division by
+ * that final scale.  The token row (and its scales) is written to each of its
+ * destination rows.  BF16: rows are copied unchanged.  Needs moe_plan_layout
+ * earlier on the same stream and workspace. */
+moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void* stream);
+
+/* Step 3 [P2 "关键源码片段" deep_gemm.py; P1 "实现拆解" 1]: for every row
+ * that carries a token: g = a W1_e^T, u = a W3_e^T (fp32 accumulation over the
+ * dequantised operands), h = silu(g) * u in fp32, stored as FP8 with 1x128
+ * UE8M0 scales (same rule as step 2) or as bf16.  Rows without a token are
+ * skipped (neither read back nor written). */
+moe_status_t moe_grouped_gemm_w13_act(moe_ctx* ctx, void* ws, void* stream);
+
+/* Step 4 [P2 "关键源码片段" deep_gemm.py]: y = h W2_e^T, fp32 accumulation,
+ * stored bf16, for rows that carry a token. */
+moe_status_t moe_grouped_gemm_w2(moe_ctx* ctx, void* ws, void* stream);
+
+/* Step 5 [P1 "风险与影响" 2 (src2dst); P3 "实现拆解" 3 (combine through slot
+ * pointers)]: out[t] = bf16(sum over j of topk_weights[t, j] * y[src2dst[t, j]])
+ * summed in fp32 in j order; 0 for tokens with no local assignment.
+ * topk_weights fp32 [T, topk], out bf16 [T, K] (device). */
+moe_status_t moe_combine(moe_ctx* ctx, const float* topk_weights, const void* ws, void* out_bf16,
+                         void* stream);
+
+/* Steps 1-5 on one stream, no synchronisation, graph-capturable. */
+moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids,
+                         const float* topk_weights, void* ws, void* out_bf16, void* stream);
+
+/* Number of kernel launches one moe_forward enqueues (for launch accounting). */
+int32_t moe_forward_launches(const moe_ctx* ctx);
+
+/* Copy the device status word to *out after synchronising stream (test use;
+ * not capturable).  moe_clear_device_status zeroes it (enqueued on stream). */
+moe_status_t moe_read_device_status(const void* ws, void* stream, int32_t* out);
+moe_status_t moe_clear_device_status(void* ws, void* stream);
+
+/* Fault-detection self-test: launches one kernel that waits on an mbarrier
+ * nothing will complete, bounded by timeout_ns; the wait gives up, writes
+ * MOE_ERR_TIMEOUT to the workspace status word and the kernel returns
+ * normally, leaving the context usable.  Enqueued on stream. */
+moe_status_t moe_selftest_wait_timeout(void* ws, int64_t timeout_ns, void* stream);
+
+/* Byte offset, inside a scale region (a_sf or h_sf), of the UE8M0 byte for
+ * (row block b, 128-column group g, row r in 0..127) when a row block holds
+ * n_groups groups.  Each (block, group) chunk is 512 bytes laid out for the
+ * tensor-memory scale copy: byte 16*(r%32) + 4*(r/32) + c, c = 0..3 (the
+ * four copies are equal).  Host helper for tests. */
+int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row);
+
+const char* moe_strerror(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,421 @@
+// C-ABI of libmoe: argument checks, workspace layout, TMA descriptors and the
+// launch sequence.  Declarations and the contract of every call are in
+// include/moe.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "internal.h"
+
+struct moe_ctx {
+  moe_shape_t shape;
+  int layout;  // resolved: MOE_LAYOUT_COMPACT or MOE_LAYOUT_MASKED
+  bool fp8;
+  const void* w13;
+  const uint8_t* w13_sf;
+  const void* w2;
+  const uint8_t* w2_sf;
+  int device;
+  int num_sms;
+  moe_ws_layout_t ws;
+  CUtensorMap map_w13;
+  CUtensorMap map_w2;
+  // descriptors of the workspace activations, rebuilt when ws moves
+  const void* ws_for_maps;
+  CUtensorMap map_a;
+  CUtensorMap map_h;
+  uint64_t timeout_ns;
+};
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// 3-D K-major tile map over [dim2][dim1][dim0] with a 128-byte inner box and
+// 128 rows, 128-byte swizzle (the layout the MMA descriptors expect).
+moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const uint64_t esize = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {dim0, dim1, dim2};
+  cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status_t check_shape(const moe_shape_t* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->K <= 0 || s->I <= 0 || s->E_global <= 0 || s->E_local <= 0 || s->expert_start < 0 ||
+      s->topk <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(s->E_local) + s->expert_start > s->E_global) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_DTYPE_FP8_E4M3_UE8M0 && s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (s->layout != MOE_LAYOUT_AUTO && s->layout != MOE_LAYOUT_COMPACT && s->layout != MOE_LAYOUT_MASKED)
+    return MOE_ERR_INVALID_ARG;
+  if (s->K % 128 || s->I % 128 || s->block_e != 128) return MOE_ERR_UNSUPPORTED;
+  if (s->E_local > moe::kMaxLocalExperts || s->topk > moe::kMaxTopk) return MOE_ERR_UNSUPPORTED;
+  if (s->T * s->topk >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+void compute_ws_layout(moe_ctx* c) {
+  const moe_shape_t& s = c->shape;
+  moe_ws_layout_t& w = c->ws;
+  memset(&w, 0, sizeof(w));
+  const int64_t A = s.T * s.topk;
+  const int64_t E = s.E_local;
+  w.layout = c->layout;
+  if (c->layout == MOE_LAYOUT_COMPACT) {
+    w.all_tokens = moe_compact_all_tokens(A, s.E_local, s.block_e);
+    w.rows = w.all_tokens;
+    w.blocks = w.all_tokens / 128;
+  } else {
+    const int64_t bpe = (s.max_m + 127) / 128;
+    w.all_tokens = 0;
+    w.rows = E * s.max_m;
+    w.blocks = E * bpe;
+  }
+  w.chunks = static_cast<int32_t>((A + moe::kPlanChunk - 1) / moe::kPlanChunk);
+  const uint64_t esize = c->fp8 ? 1 : 2;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = align_up(off + (bytes ? bytes : 1), 1024);
+    return o;
+  };
+  w.status = take(16);
+  w.meta = take(32);
+  w.counts = take(4 * E);
+  w.padded = take(4 * E);
+  w.start = take(4 * E);
+  w.masked_m = take(4 * E);
+  w.m_indices = take(4 * static_cast<uint64_t>(w.all_tokens));
+  w.src2dst = take(4 * static_cast<uint64_t>(A));
+  w.block_info = take(16 * static_cast<uint64_t>(w.blocks));
+  w.chunk_hist = take(4 * static_cast<uint64_t>(w.chunks) * E);
+  w.chunk_rank = take(4 * static_cast<uint64_t>(A));
+  w.a = take(static_cast<uint64_t>(w.rows) * s.K * esize);
+  w.a_sf = take(c->fp8 ? static_cast<uint64_t>(w.blocks) * (s.K / 128) * 512 : 0);
+  w.h = take(static_cast<uint64_t>(w.rows) * s.I * esize);
+  w.h_sf = take(c->fp8 ? static_cast<uint64_t>(w.blocks) * (s.I / 128) * 512 : 0);
+  w.y = take(static_cast<uint64_t>(w.rows) * s.K * 2);
+  w.total_bytes = off;
+}
+
+template <typename T>
+T* at(void* ws, uint64_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_ws(const moe_ctx* c, const void* ws) {
+  if (!c || !ws) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_MISALIGNED;
+  return MOE_OK;
+}
+
+moe_status_t ensure_ws_maps(moe_ctx* c, void* ws) {
+  if (c->ws_for_maps == ws) return MOE_OK;
+  const moe_shape_t& s = c->shape;
+  const bool masked = c->layout == MOE_LAYOUT_MASKED;
+  const uint64_t d1 = masked ? static_cast<uint64_t>(s.max_m) : static_cast<uint64_t>(c->ws.rows);
+  const uint64_t d2 = masked ? static_cast<uint64_t>(s.E_local) : 1;
+  if (c->ws.rows > 0) {
+    moe_status_t st = make_map(&c->map_a, at<uint8_t>(ws, c->ws.a), c->fp8, s.K, d1, d2);
+    if (st != MOE_OK) return st;
+    st = make_map(&c->map_h, at<uint8_t>(ws, c->ws.h), c->fp8, s.I, d1, d2);
+    if (st != MOE_OK) return st;
+  }
+  c->ws_for_maps = ws;
+  return MOE_OK;
+}
+
+moe::GemmArgs gemm_args(const moe_ctx* c, void* ws, int stage) {
+  const moe_shape_t& s = c->shape;
+  moe::GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.block_info = at<int32_t>(ws, c->ws.block_info);
+  g.meta = at<int32_t>(ws, c->ws.meta);
+  g.status = at<int32_t>(ws, c->ws.status);
+  g.stage = stage;
+  g.fp8 = c->fp8;
+  g.masked = c->layout == MOE_LAYOUT_MASKED;
+  g.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
+  const int64_t red = stage == 1 ? s.K : s.I;
+  g.k_blocks = static_cast<int32_t>(red / (c->fp8 ? 128 : 64));
+  g.timeout_ns = c->timeout_ns;
+  if (stage == 1) {
+    g.n_blocks = static_cast<int32_t>(s.I / 128);
+    g.n_half = s.I;
+    g.n_total = s.I;
+    g.w_rows_blocks = static_cast<int32_t>(2 * s.I / 128);
+    g.w_k_groups = static_cast<int32_t>(s.K / 128);
+    g.a_sf = at<uint8_t>(ws, c->ws.a_sf);
+    g.w_sf = c->w13_sf;
+    g.out = at<void>(ws, c->ws.h);
+    g.out_ld = s.I;
+    g.out_sf = at<uint8_t>(ws, c->ws.h_sf);
+    g.out_groups = static_cast<int32_t>(s.I / 128);
+  } else {
+    g.n_blocks = static_cast<int32_t>((s.K + 255) / 256);
+    g.n_half = 0;
+    g.n_total = s.K;
+    g.w_rows_blocks = static_cast<int32_t>(s.K / 128);
+    g.w_k_groups = static_cast<int32_t>(s.I / 128);
+    g.a_sf = at<uint8_t>(ws, c->ws.h_sf);
+    g.w_sf = c->w2_sf;
+    g.out = at<void>(ws, c->ws.y);
+    g.out_ld = s.K;
+  }
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_compact_all_tokens(int64_t num_assignments, int32_t num_experts, int32_t block_e) {
+  if (num_assignments < 0 || num_experts < 0 || block_e <= 0) return -1;
+  const int64_t nonempty = num_assignments < num_experts ? num_assignments : num_experts;
+  return static_cast<int64_t>(block_e) * (nonempty + (num_assignments - nonempty) / block_e);
+}
+
+int32_t moe_choose_layout(int32_t E_global, int32_t E_local) {
+  return (E_global > E_local && E_local <= 32) ? MOE_LAYOUT_MASKED : MOE_LAYOUT_COMPACT;
+}
+
+moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uint8_t* w13_sf, const void* w2,
+                            const uint8_t* w2_sf, moe_ctx** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const bool fp8 = shape->dtype == MOE_DTYPE_FP8_E4M3_UE8M0;
+  if (!w13 || !w2) return MOE_ERR_INVALID_ARG;
+  if (fp8 != (w13_sf != nullptr) || fp8 != (w2_sf != nullptr)) return MOE_ERR_DTYPE_MISMATCH;
+  if (!aligned16(w13) || !aligned16(w2)) return MOE_ERR_MISALIGNED;
+  int layout = shape->layout == MOE_LAYOUT_AUTO ? moe_choose_layout(shape->E_global, shape->E_local) : shape->layout;
+  if (layout == MOE_LAYOUT_MASKED && shape->max_m < (shape->T > 0 ? shape->T : 1)) return MOE_ERR_INVALID_ARG;
+  if (layout == MOE_LAYOUT_MASKED && static_cast<int64_t>(shape->E_local) * shape->max_m >= (int64_t(1) << 31))
+    return MOE_ERR_UNSUPPORTED;
+
+  moe_ctx* c = new (std::nothrow) moe_ctx;
+  if (!c) return MOE_ERR_INVALID_ARG;
+  memset(c, 0, sizeof(*c));
+  c->shape = *shape;
+  c->shape.layout = layout;
+  c->layout = layout;
+  c->fp8 = fp8;
+  c->w13 = w13;
+  c->w13_sf = w13_sf;
+  c->w2 = w2;
+  c->w2_sf = w2_sf;
+  c->timeout_ns = 2000000000ull;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  compute_ws_layout(c);
+  st = make_map(&c->map_w13, w13, fp8, shape->K, 2 * shape->I, shape->E_local);
+  if (st == MOE_OK) st = make_map(&c->map_w2, w2, fp8, shape->I, shape->K, shape->E_local);
+  if (st != MOE_OK) {
+    delete c;
+    return st;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+void moe_ctx_destroy(moe_ctx* ctx) { delete ctx; }
+
+moe_status_t moe_workspace_layout(const moe_ctx* ctx, moe_ws_layout_t* out) {
+  if (!ctx || !out) return MOE_ERR_INVALID_ARG;
+  *out = ctx->ws;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size(const moe_ctx* ctx, size_t* bytes) {
+  if (!ctx || !bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = static_cast<size_t>(ctx->ws.total_bytes);
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, void* stream) {
+  moe_status_t st = check_ws(ctx, ws);
+  if (st != MOE_OK) return st;
+  const moe_shape_t& s = ctx->shape;
+  const int64_t A = s.T * s.topk;
+  if (A > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
+  if (topk_ids && !aligned16(topk_ids)) return MOE_ERR_MISALIGNED;
+  moe::PlanArgs p;
+  memset(&p, 0, sizeof(p));
+  p.topk_ids = topk_ids;
+  p.A = A;
+  p.E_global = s.E_global;
+  p.E_local = s.E_local;
+  p.expert_start = s.expert_start;
+  p.masked = ctx->layout == MOE_LAYOUT_MASKED;
+  p.max_m = s.max_m;
+  p.all_tokens = ctx->ws.all_tokens;
+  p.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
+  p.chunks = ctx->ws.chunks;
+  p.status = at<int32_t>(ws, ctx->ws.status);
+  p.meta = at<int32_t>(ws, ctx->ws.meta);
+  p.counts = at<int32_t>(ws, ctx->ws.counts);
+  p.padded = at<int32_t>(ws, ctx->ws.padded);
+  p.start = at<int32_t>(ws, ctx->ws.start);
+  p.masked_m = at<int32_t>(ws, ctx->ws.masked_m);
+  p.m_indices = at<int32_t>(ws, ctx->ws.m_indices);
+  p.src2dst = at<int32_t>(ws, ctx->ws.src2dst);
+  p.block_info = at<int32_t>(ws, ctx->ws.block_info);
+  p.chunk_hist = at<int32_t>(ws, ctx->ws.chunk_hist);
+  p.chunk_rank = at<int32_t>(ws, ctx->ws.chunk_rank);
+  return cuda_status(moe::launch_plan(p, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void* stream) {
+  moe_status_t st = check_ws(ctx, ws);
+  if (st != MOE_OK) return st;
+  const moe_shape_t& s = ctx->shape;
+  if (s.T > 0 && !x_bf16) return MOE_ERR_INVALID_ARG;
+  if (x_bf16 && !aligned16(x_bf16)) return MOE_ERR_MISALIGNED;
+  moe::QuantArgs q;
+  memset(&q, 0, sizeof(q));
+  q.x = x_bf16;
+  q.src2dst = at<int32_t>(ws, ctx->ws.src2dst);
+  q.T = s.T;
+  q.K = s.K;
+  q.topk = s.topk;
+  q.fp8 = ctx->fp8;
+  q.masked = ctx->layout == MOE_LAYOUT_MASKED;
+  q.max_m = s.max_m;
+  q.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
+  q.a = at<void>(ws, ctx->ws.a);
+  q.a_sf = at<uint8_t>(ws, ctx->ws.a_sf);
+  return cuda_status(moe::launch_quant_scatter(q, static_cast<cudaStream_t>(stream)));
+}
+
+static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
+  moe_status_t st = check_ws(ctx, ws);
+  if (st != MOE_OK) return st;
+  if (ctx->ws.blocks == 0) return MOE_OK;
+  st = ensure_ws_maps(ctx, ws);
+  if (st != MOE_OK) return st;
+  const moe::GemmArgs g = gemm_args(ctx, ws, stage);
+  int64_t max_tiles = ctx->ws.blocks * g.n_blocks;
+  int grid = ctx->num_sms;
+  if (max_tiles < grid) grid = static_cast<int>(max_tiles);
+  const CUtensorMap& a = stage == 1 ? ctx->map_a : ctx->map_h;
+  const CUtensorMap& b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
+  return cuda_status(moe::launch_gemm(g, a, b, grid, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_grouped_gemm_w13_act(moe_ctx* ctx, void* ws, void* stream) { return run_gemm(ctx, ws, stream, 1); }
+
+moe_status_t moe_grouped_gemm_w2(moe_ctx* ctx, void* ws, void* stream) { return run_gemm(ctx, ws, stream, 2); }
+
+moe_status_t moe_combine(moe_ctx* ctx, const float* topk_weights, const void* ws, void* out_bf16, void* stream) {
+  moe_status_t st = check_ws(ctx, ws);
+  if (st != MOE_OK) return st;
+  const moe_shape_t& s = ctx->shape;
+  if (s.T > 0 && (!topk_weights || !out_bf16)) return MOE_ERR_INVALID_ARG;
+  if ((topk_weights && !aligned16(topk_weights)) || (out_bf16 && !aligned16(out_bf16))) return MOE_ERR_MISALIGNED;
+  moe::CombineArgs c;
+  c.y = at<const void>(const_cast<void*>(ws), ctx->ws.y);
+  c.src2dst = at<const int32_t>(const_cast<void*>(ws), ctx->ws.src2dst);
+  c.topk_weights = topk_weights;
+  c.T = s.T;
+  c.K = s.K;
+  c.topk = s.topk;
+  c.out = out_bf16;
+  return cuda_status(moe::launch_combine(c, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                         void* ws, void* out_bf16, void* stream) {
+  moe_status_t st;
+  if ((st = moe_plan_layout(ctx, topk_ids, ws, stream)) != MOE_OK) return st;
+  if ((st = moe_quant_scatter(ctx, x_bf16, ws, stream)) != MOE_OK) return st;
+  if ((st = moe_grouped_gemm_w13_act(ctx, ws, stream)) != MOE_OK) return st;
+  if ((st = moe_grouped_gemm_w2(ctx, ws, stream)) != MOE_OK) return st;
+  return moe_combine(ctx, topk_weights, ws, out_bf16, stream);
+}
+
+int32_t moe_forward_launches(const moe_ctx* ctx) {
+  if (!ctx) return -1;
+  const moe_shape_t& s = ctx->shape;
+  int n = (ctx->ws.chunks > 0 ? 1 : 0) + 2;  // plan
+  if (s.T > 0) n += 2;                          // quant + combine
+  if (ctx->ws.blocks > 0) n += 2;               // two GEMMs
+  return n;
+}
+
+moe_status_t moe_read_device_status(const void* ws, void* stream, int32_t* out) {
+  if (!ws || !out) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(cudaMemcpy(out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost));
+}
+
+moe_status_t moe_clear_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(ws, 0, 16, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_selftest_wait_timeout(void* ws, int64_t timeout_ns, void* stream) {
+  if (!ws || timeout_ns <= 0) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_selftest_wait(static_cast<int32_t*>(ws), static_cast<uint64_t>(timeout_ns),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {
+  return moe::sf_chunk_offset(block, group, n_groups) + moe::sf_row_offset(row);
+}
+
+const char* moe_strerror(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case MOE_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_EXPERT_ID: return "expert id outside [-1, E_global)";
+    case MOE_ERR_MASKED_OVERFLOW: return "masked expert received more than max_m rows";
+    case MOE_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
+    case MOE_ERR_DTYPE_MISMATCH: return "weights contradict the declared dtype";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kPlanChunk = 256;   // assignments per plan CTA (8 warps x 32)
+constexpr int kMaxLocalExperts = 1024;
+constexpr int kMaxTopk = 64;
+constexpr int kBlockM = 128;      // rows per expert block == compact block_e
+
+struct PlanArgs {
+  const int32_t* topk_ids;  // [A]
+  int64_t A;                // T * topk
+  int32_t E_global, E_local, expert_start;
+  int32_t masked;           // 0 compact, 1 masked
+  int64_t max_m;            // masked rows per expert
+  int64_t all_tokens;       // compact static bound
+  int32_t blocks_per_expert;  // masked: ceil(max_m / 128)
+  int32_t chunks;
+  int32_t* status;
+  int32_t* meta;
+  int32_t* counts;
+  int32_t* padded;
+  int32_t* start;
+  int32_t* masked_m;
+  int32_t* m_indices;
+  int32_t* src2dst;
+  int32_t* block_info;      // int4 per block
+  int32_t* chunk_hist;      // [chunks, E_local]
+  int32_t* chunk_rank;      // [A]
+};
+
+struct QuantArgs {
+  const void* x;            // bf16 [T, K]
+  const int32_t* src2dst;   // [T, topk]
+  int64_t T, K;
+  int32_t topk;
+  int32_t fp8;
+  int32_t masked;
+  int64_t max_m;
+  int32_t blocks_per_expert;
+  void* a;                  // fp8 or bf16 [rows, K]
+  uint8_t* a_sf;            // scale chunks
+};
+
+struct CombineArgs {
+  const void* y;            // bf16 [rows, K]
+  const int32_t* src2dst;
+  const float* topk_weights;
+  int64_t T, K;
+  int32_t topk;
+  void* out;                // bf16 [T, K]
+};
+
+// One grouped GEMM launch (either stage).
+struct GemmArgs {
+  const int32_t* block_info;  // int4 {expert, row0, tma_row0, valid}
+  const int32_t* meta;        // meta[1] = valid blocks
+  int32_t* status;
+  int32_t stage;              // 1: w13 + SiLU*up, 2: w2
+  int32_t fp8;
+  int32_t masked;
+  int32_t blocks_per_expert;  // masked
+  int32_t n_blocks;           // output column blocks (128 h columns, or 256 y columns)
+  int32_t k_blocks;           // 128-byte K blocks of the reduction
+  int64_t n_half;             // stage 1: I (row offset of the up projection in w13)
+  int64_t n_total;            // output columns (I for stage 1, K for stage 2)
+  int32_t w_rows_blocks;      // weight rows / 128 (for the weight-scale table)
+  int32_t w_k_groups;         // reduction / 128 (weight-scale table)
+  const uint8_t* a_sf;        // fp8: activation scale chunks
+  const uint8_t* w_sf;        // fp8: weight scales [E, rows/128, red/128]
+  void* out;                  // h (stage 1) or y (stage 2)
+  int64_t out_ld;             // output row stride in elements
+  uint8_t* out_sf;            // stage 1 fp8: h scale chunks
+  int32_t out_groups;         // stage 1 fp8: I / 128
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
+cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUtensorMap& map_b, int grid,
+                        cudaStream_t s);
+cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
+
+int plan_launches();
+int gemm_smem_bytes(int fp8);
+
+}  // namespace moe

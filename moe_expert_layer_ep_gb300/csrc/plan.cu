@@ -1,0 +1,217 @@
+// moe_plan_layout: top-k routing -> per-expert row layout.
+//
+// "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
+// "实现拆解" steps 2-3 and "关键源码片段" ep_moe_kernels.py: experts are laid
+// out one after another, each padded to a multiple of 128 rows; the first
+// `valid` rows of an expert's range carry its tokens and the rest are marked
+// -1 in m_indices.  "[Feature] Support BF16 and batch-invariant inference
+// with DeepEP v2" (sglang PR #38160 report), "实现拆解" step 1: only ids in
+// [expert_start, expert_start + E_local) are local.
+//
+// Destination rows follow the flattened t * topk + j order inside each expert
+// (a stable counting sort), which makes the layout deterministic and
+// independent of thread scheduling:
+//   1. plan_count_rank  one CTA per 256 assignments: per-expert counts of the
+//                       chunk and each assignment's rank inside the chunk
+//                       (warp match + per-warp counts; integer only).
+//   2. plan_scan        one CTA: per-expert exclusive scan over chunks, padded
+//                       sizes, expert starts, the 128-row block table.
+//   3. plan_finalize    src2dst = start + chunk offset + rank; m_indices.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+__device__ __forceinline__ int local_expert(int32_t gid, int32_t E_global, int32_t E_local, int32_t expert_start,
+                                            bool* bad) {
+  *bad = (gid < -1) || (gid >= E_global);
+  if (*bad || gid < 0) return -1;
+  const int e = gid - expert_start;
+  return (e >= 0 && e < E_local) ? e : -1;
+}
+
+__global__ void __launch_bounds__(kPlanChunk) plan_count_rank(PlanArgs p) {
+  extern __shared__ int32_t s_wcnt[];  // [8 warps][E_local]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E_local;
+  for (int i = tid; i < 8 * E; i += kPlanChunk) s_wcnt[i] = 0;
+  __syncthreads();
+
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kPlanChunk + tid;
+  int e = -1;
+  if (i < p.A) {
+    bool bad;
+    e = local_expert(p.topk_ids[i], p.E_global, p.E_local, p.expert_start, &bad);
+    if (bad) set_status(p.status, MOE_ERR_EXPERT_ID);
+  }
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+  const unsigned lower = peers & ((1u << lane) - 1u);
+  if (e >= 0 && lower == 0) s_wcnt[warp * E + e] = __popc(peers);
+  __syncthreads();
+  if (e >= 0) {
+    int prefix = 0;
+    for (int w = 0; w < warp; ++w) prefix += s_wcnt[w * E + e];
+    p.chunk_rank[i] = prefix + __popc(lower);
+  }
+  for (int x = tid; x < E; x += kPlanChunk) {
+    int total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) total += s_wcnt[w * E + x];
+    p.chunk_hist[static_cast<int64_t>(blockIdx.x) * E + x] = total;
+  }
+}
+
+// Exclusive scan over a 1024-thread block; returns this thread's prefix and
+// writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int warp_base = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[31];
+  __syncthreads();
+  return warp_base + x - v;
+}
+
+__global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  const bool act = e < p.E_local;
+  int count = 0;
+  if (act) {
+    for (int c = 0; c < p.chunks; ++c) {
+      int32_t* cell = p.chunk_hist + static_cast<int64_t>(c) * p.E_local + e;
+      const int v = *cell;
+      *cell = count;  // becomes the chunk's exclusive offset inside expert e
+      count += v;
+    }
+  }
+  int rows, nblk;
+  if (!p.masked) {
+    rows = (count + kBlockM - 1) / kBlockM * kBlockM;
+    nblk = rows / kBlockM;
+  } else {
+    if (count > p.max_m) set_status(p.status, MOE_ERR_MASKED_OVERFLOW);
+    rows = count < p.max_m ? count : static_cast<int>(p.max_m);
+    nblk = (rows + kBlockM - 1) / kBlockM;
+  }
+  int total_rows, total_blk;
+  const int row_start = block_exclusive_scan(act ? rows : 0, s_warp, &total_rows);
+  const int blk_start = block_exclusive_scan(act ? nblk : 0, s_warp, &total_blk);
+  if (act) {
+    p.counts[e] = count;
+    if (!p.masked) {
+      p.padded[e] = rows;
+      p.start[e] = row_start;
+    } else {
+      p.masked_m[e] = rows;
+    }
+    for (int b = 0; b < nblk; ++b) {
+      int4 info;
+      info.x = e;
+      if (!p.masked) {
+        info.y = row_start + b * kBlockM;
+        info.z = info.y;
+        const int left = count - b * kBlockM;
+        info.w = left < kBlockM ? left : kBlockM;
+      } else {
+        info.y = static_cast<int>(static_cast<int64_t>(e) * p.max_m + b * kBlockM);
+        info.z = b * kBlockM;
+        const int left = rows - b * kBlockM;
+        info.w = left < kBlockM ? left : kBlockM;
+      }
+      reinterpret_cast<int4*>(p.block_info)[blk_start + b] = info;
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.meta[0] = total_rows;
+    p.meta[1] = total_blk;
+  }
+}
+
+__global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
+  extern __shared__ int32_t s_tab[];  // start[E], padded[E], counts[E] (compact)
+  const int E = p.E_local;
+  if (!p.masked) {
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+      s_tab[x] = p.start[x];
+      s_tab[E + x] = p.padded[x];
+      s_tab[2 * E + x] = p.counts[x];
+    }
+    __syncthreads();
+  }
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.A; i += stride) {
+    bool bad;
+    const int e = local_expert(p.topk_ids[i], p.E_global, p.E_local, p.expert_start, &bad);
+    int32_t dst = -1;
+    if (e >= 0) {
+      const int rank = p.chunk_hist[(i / kPlanChunk) * E + e] + p.chunk_rank[i];
+      if (!p.masked) {
+        dst = s_tab[e] + rank;
+      } else if (rank < p.max_m) {
+        dst = static_cast<int32_t>(static_cast<int64_t>(e) * p.max_m + rank);
+      }
+    }
+    p.src2dst[i] = dst;
+  }
+  if (!p.masked) {
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < p.all_tokens; r += stride) {
+      // last expert whose start is <= r (empty experts share starts; the
+      // last one with that start owns the rows)
+      int lo = 0, hi = E - 1, found = -1;
+      while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tab[mid] <= r) {
+          found = mid;
+          lo = mid + 1;
+        } else {
+          hi = mid - 1;
+        }
+      }
+      int32_t v = -1;
+      if (found >= 0) {
+        const int64_t off = r - s_tab[found];
+        if (off < s_tab[E + found] && off < s_tab[2 * E + found]) v = found;
+      }
+      p.m_indices[r] = v;
+    }
+  }
+}
+
+}  // namespace
+
+int plan_launches() { return 3; }
+
+cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s) {
+  if (p.chunks > 0) {
+    plan_count_rank<<<p.chunks, kPlanChunk, 8 * p.E_local * sizeof(int32_t), s>>>(p);
+  }
+  plan_scan<<<1, 1024, 0, s>>>(p);
+  const int64_t work = p.A > p.all_tokens ? p.A : p.all_tokens;
+  int grid = static_cast<int>((work + 255) / 256);
+  if (grid > 1184) grid = 1184;
+  if (grid < 1) grid = 1;
+  plan_finalize<<<grid, 256, 3 * p.E_local * sizeof(int32_t), s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,182 @@
+// moe_quant_scatter: token rows -> expert rows, FP8 1x128 UE8M0 or BF16.
+//
+// "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
+// "实现拆解" step 3: activations are quantised directly with a power-of-two
+// (UE8M0) scale rather than quantised with a real scale whose value is
+// rounded afterwards.  For each 128-column group the exponent is the smallest
+// s with amax <= 448 * 2^s; every element is multiplied by 2^-s (exact) and
+// rounded to e4m3 (nearest even, saturating).  "Add BF16 support to EP-MoE for
+// DeepGEMM" (sglang PR #17392 report), "实现拆解" step 3: the BF16 path moves
+// the rows without scales.
+//
+// One CTA per token: the row is read once (16-byte loads, 8 columns per
+// thread, a 128-column group = 16 consecutive lanes), quantised once, and
+// written to each of the token's destination rows (8-byte FP8 / 16-byte BF16
+// stores, coalesced per group).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kQuantThreads = 256;
+constexpr int kColsPerIter = kQuantThreads * 8;
+
+__device__ __forceinline__ void dest_block(const QuantArgs& q, int64_t d, int64_t* block, int* row) {
+  if (!q.masked) {
+    *block = d >> 7;
+    *row = static_cast<int>(d & 127);
+  } else {
+    const int64_t e = d / q.max_m;
+    const int64_t pos = d - e * q.max_m;
+    *block = e * q.blocks_per_expert + (pos >> 7);
+    *row = static_cast<int>(pos & 127);
+  }
+}
+
+template <bool kFP8>
+__global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs q) {
+  __shared__ int64_t s_dst[kMaxTopk];
+  __shared__ int64_t s_blk[kMaxTopk];
+  __shared__ int s_row[kMaxTopk];
+  __shared__ int s_any;
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_any = 0;
+  __syncthreads();
+  if (tid < q.topk) {
+    const int64_t d = q.src2dst[t * q.topk + tid];
+    s_dst[tid] = d;
+    if (d >= 0) {
+      s_any = 1;
+      dest_block(q, d, &s_blk[tid], &s_row[tid]);
+    }
+  }
+  __syncthreads();
+  if (!s_any) return;
+
+  const uint16_t* xrow = static_cast<const uint16_t*>(q.x) + t * q.K;
+  const int64_t n_groups = q.K / 128;
+  for (int64_t c0 = 0; c0 < q.K; c0 += kColsPerIter) {
+    const int64_t col = c0 + static_cast<int64_t>(tid) * 8;
+    const bool active = col < q.K;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (active) v = __ldg(reinterpret_cast<const uint4*>(xrow + col));
+    if constexpr (kFP8) {
+      float f[8];
+      const float2 p0 = unpack_bf16x2(v.x), p1 = unpack_bf16x2(v.y), p2 = unpack_bf16x2(v.z),
+                   p3 = unpack_bf16x2(v.w);
+      f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
+      f[4] = p2.x; f[5] = p2.y; f[6] = p3.x; f[7] = p3.y;
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      // 16 lanes = one 128-column group
+#pragma unroll
+      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const int s = ue8m0_exponent(amax);
+      const float mul = exp2_neg(s);
+      uint2 packed;
+      packed.x = cvt_e4m3x2(f[0] * mul, f[1] * mul) | (cvt_e4m3x2(f[2] * mul, f[3] * mul) << 16);
+      packed.y = cvt_e4m3x2(f[4] * mul, f[5] * mul) | (cvt_e4m3x2(f[6] * mul, f[7] * mul) << 16);
+      if (active) {
+        const uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
+        const int64_t group = col >> 7;
+        const bool group_lead = (tid & 15) == 0;
+        for (int j = 0; j < q.topk; ++j) {
+          const int64_t d = s_dst[j];
+          if (d < 0) continue;
+          uint8_t* arow = static_cast<uint8_t*>(q.a) + d * q.K;
+          *reinterpret_cast<uint2*>(arow + col) = packed;
+          if (group_lead) {
+            *reinterpret_cast<uint32_t*>(q.a_sf + sf_chunk_offset(s_blk[j], group, n_groups) +
+                                         sf_row_offset(s_row[j])) = sf_word;
+          }
+        }
+      }
+    } else {
+      if (active) {
+        for (int j = 0; j < q.topk; ++j) {
+          const int64_t d = s_dst[j];
+          if (d < 0) continue;
+          uint16_t* arow = static_cast<uint16_t*>(q.a) + d * q.K;
+          *reinterpret_cast<uint4*>(arow + col) = v;
+        }
+      }
+    }
+  }
+}
+
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs c) {
+  __shared__ int64_t s_dst[kMaxTopk];
+  __shared__ float s_w[kMaxTopk];
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid < c.topk) {
+    s_dst[tid] = c.src2dst[t * c.topk + tid];
+    s_w[tid] = c.topk_weights[t * c.topk + tid];
+  }
+  __syncthreads();
+  const uint16_t* y = static_cast<const uint16_t*>(c.y);
+  uint16_t* orow = static_cast<uint16_t*>(c.out) + t * c.K;
+  for (int64_t col = static_cast<int64_t>(tid) * 8; col < c.K; col += kCombineThreads * 8) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int j0 = 0; j0 < c.topk; j0 += 8) {
+      uint4 v[8];
+      // issue all loads of the batch before using them
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        v[jj] = make_uint4(0, 0, 0, 0);
+        if (j < c.topk && s_dst[j] >= 0) v[jj] = *reinterpret_cast<const uint4*>(y + s_dst[j] * c.K + col);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = j0 + jj;
+        if (j < c.topk && s_dst[j] >= 0) {
+          const float w = s_w[j];
+          const float2 p0 = unpack_bf16x2(v[jj].x), p1 = unpack_bf16x2(v[jj].y), p2 = unpack_bf16x2(v[jj].z),
+                       p3 = unpack_bf16x2(v[jj].w);
+          acc[0] = fmaf(w, p0.x, acc[0]);
+          acc[1] = fmaf(w, p0.y, acc[1]);
+          acc[2] = fmaf(w, p1.x, acc[2]);
+          acc[3] = fmaf(w, p1.y, acc[3]);
+          acc[4] = fmaf(w, p2.x, acc[4]);
+          acc[5] = fmaf(w, p2.y, acc[5]);
+          acc[6] = fmaf(w, p3.x, acc[6]);
+          acc[7] = fmaf(w, p3.y, acc[7]);
+        }
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(orow + col) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s) {
+  if (q.T <= 0) return cudaSuccess;
+  if (q.fp8)
+    quant_scatter_kernel<true><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
+  else
+    quant_scatter_kernel<false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s) {
+  if (c.T <= 0) return cudaSuccess;
+  combine_kernel<<<static_cast<unsigned>(c.T), kCombineThreads, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -38,6 +38,7 @@ from .formats import (  # noqa: F401
     e4m3_from_bits,
     ue8m0_exponent,
     quant_fp8_1x128,
+    dequant_1x128,
 )
 from .layout import (  # noqa: F401
     compact_all_tokens,
@@ -45,8 +46,12 @@ from .layout import (  # noqa: F401
     plan_layout,
 )
 from .moe import (  # noqa: F401
+    combine,
     dequant_fp8_weights,
     expert_ffn,
+    gemm1_act,
+    gemm2,
+    store_act,
     forward_layout,
     forward_per_token,
     silu,

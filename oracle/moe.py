@@ -51,7 +51,7 @@ def dequant_fp8_weights(w_bytes, w_exp):
     return (w.reshape(E, N // 128, 128, C // 128, 128) * scale[:, :, None, :, None]).reshape(E, N, C)
 
 
-def _store_act(x, dtype):
+def store_act(x, dtype):
     """Quantise activation rows to the GEMM input format; returns the fp64
     values the GEMM consumes and, for FP8, the (q, s) pair."""
     if dtype == "fp8":
@@ -63,15 +63,41 @@ def _store_act(x, dtype):
     raise ValueError(dtype)
 
 
+def gemm1_act(a, w13_e):
+    """GEMM1 + activation on rows a [R, K] (fp64 values in the GEMM input
+    format): returns (g, u, h) with h = silu(g) * u, all unrounded fp64."""
+    I = w13_e.shape[0] // 2
+    g = a @ w13_e[:I].T
+    u = a @ w13_e[I:].T
+    return g, u, silu(g) * u
+
+
+def gemm2(h_in, w2_e):
+    """GEMM2 on rows h_in [R, I] (stored h values): y = h W2^T rounded to bf16."""
+    return bf16_round(h_in @ w2_e.T)
+
+
+def combine(y, src2dst, topk_weights):
+    """out[t] = bf16(sum_j w[t, j] * y[src2dst[t, j]]) over j with src2dst >= 0,
+    summed in fp64 in j order; tokens with no destination get 0."""
+    T, k = src2dst.shape
+    out = np.zeros((T, y.shape[1]))
+    for t in range(T):
+        acc = np.zeros(y.shape[1])
+        for j in range(k):
+            d = src2dst[t, j]
+            if d >= 0:
+                acc = acc + float(topk_weights[t, j]) * y[d]
+        out[t] = bf16_round(acc)
+    return out
+
+
 def expert_ffn(a, w13_e, w2_e, dtype, keep=False):
     """One expert on rows ``a`` [R, K] (already in the GEMM input format,
     fp64 values).  w13_e [2I, K], w2_e [K, I] fp64.  Returns y [R, K] (bf16
     values) and, with keep=True, a dict of the intermediates."""
-    I = w13_e.shape[0] // 2
-    g = a @ w13_e[:I].T
-    u = a @ w13_e[I:].T
-    h = silu(g) * u
-    h_in, h_stored = _store_act(h, dtype)
+    g, u, h = gemm1_act(a, w13_e)
+    h_in, h_stored = store_act(h, dtype)
     y_acc = h_in @ w2_e.T
     y = bf16_round(y_acc)
     if keep:
@@ -111,7 +137,7 @@ def forward_layout(x, w13, w2, topk_ids, topk_weights, dtype, E_global, expert_s
     rows = plan["all_tokens"] if layout == "compact" else E_l * max_m
 
     # 2. quantise each token once, then scatter it to all its destination rows
-    x_in, x_stored = _store_act(x, dtype)
+    x_in, x_stored = store_act(x, dtype)
     a = np.full((rows, K), np.nan)          # rows without a token stay undefined
     for t in range(T):
         for j in range(topk_ids.shape[1]):
@@ -134,14 +160,7 @@ def forward_layout(x, w13, w2, topk_ids, topk_weights, dtype, E_global, expert_s
         h_in[r] = inter["h_in"]
 
     # 5. weighted combine in token order, fixed j order
-    out = np.zeros((T, K))
-    for t in range(T):
-        acc = np.zeros(K)
-        for j in range(topk_ids.shape[1]):
-            d = src2dst[t, j]
-            if d >= 0:
-                acc = acc + topk_weights[t, j] * y[d]
-        out[t] = bf16_round(acc)
+    out = combine(y, src2dst, topk_weights)
     if keep:
         return out, {"plan": plan, "layout": layout, "x_in": x_in, "x_stored": x_stored,
                      "a": a, "h_in": h_in, "y": y, "max_m": max_m}
@@ -157,7 +176,7 @@ def forward_per_token(x, w13, w2, topk_ids, topk_weights, dtype, E_global, exper
     T, K, E_l, I = _check_shapes(x, w13, w2, topk_ids, topk_weights)
     out = np.zeros((T, K))
     for t in range(T):
-        x_t, _ = _store_act(x[t:t + 1], dtype)
+        x_t, _ = store_act(x[t:t + 1], dtype)
         acc = np.zeros(K)
         for j in range(topk_ids.shape[1]):
             gid = int(topk_ids[t, j])

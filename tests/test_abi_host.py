@@ -1,0 +1,51 @@
+"""C-ABI checks that need no GPU: libmoe loads, exports every function that
+include/moe.h declares, and its host-only helpers agree with the oracle."""
+
+import os
+import re
+
+import numpy as np
+
+import oracle
+import moe_expert_layer_ep_gb300 as M
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(M._lib, n), n
+        assert n in M.EXPORTED, n
+
+
+def test_compact_bound_and_layout_choice_match_oracle():
+    rng = np.random.default_rng(0)
+    for _ in range(500):
+        A = int(rng.integers(0, 100000))
+        E = int(rng.integers(1, 1025))
+        assert M.moe_compact_all_tokens(A, E, 128) == oracle.compact_all_tokens(A, E, 128)
+    for eg in (8, 32, 64, 256):
+        for el in (1, 8, 32, 33, 64, 256):
+            if el <= eg:
+                expect = M.MOE_LAYOUT_MASKED if oracle.use_masked_layout(eg, el) else M.MOE_LAYOUT_COMPACT
+                assert M.moe_choose_layout(eg, el) == expect
+    assert M.moe_compact_all_tokens(-1, 4, 128) == -1
+
+
+def test_scale_chunk_offsets_are_a_bijection():
+    offs = {M.moe_sf_offset(b, g, 3, r) for b in range(2) for g in range(3) for r in range(128)}
+    assert len(offs) == 2 * 3 * 128
+    assert all(o % 4 == 0 and 0 <= o < 2 * 3 * 512 for o in offs)
+
+
+def test_status_strings():
+    for code in M.STATUS_NAMES:
+        assert M._lib.moe_strerror(code)
