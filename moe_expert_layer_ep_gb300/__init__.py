@@ -4,7 +4,8 @@ Argument marshalling only: every step of the layer runs in libmoe's CUDA
 kernels; this module turns torch tensors into device pointers and the current
 torch stream into a cudaStream_t, and raises on error codes.  PyTorch supplies
 device memory and streams.  Importing fails loudly when libmoe.so has not
-been built (run ``python -m moe_expert_layer_ep_gb300.build``); there is no
+been built (run ``python moe_expert_layer_ep_gb300/build.py`` or
+``__graft_entry__.build()``); there is no
 fallback implementation.
 
 The C functions and their contracts are declared in include/moe.h; the
@@ -58,7 +59,7 @@ class MoeWsLayout(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run python -m moe_expert_layer_ep_gb300.build")
+        raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run python moe_expert_layer_ep_gb300/build.py")
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     sig = {

@@ -1,5 +1,5 @@
 """Build libmoe.so in-tree for sm_103a with nvcc (translation units compiled in
-parallel, one -gencode).  Usage: python -m moe_expert_layer_ep_gb300.build"""
+parallel, one -gencode).  Usage: python moe_expert_layer_ep_gb300/build.py [-v]"""
 
 import os
 import shutil
