@@ -26,9 +26,10 @@
  * - Errors the host can see (bad pointers, sizes, unsupported shapes) are
  *   returned before anything is launched.  Errors in the data (an expert id
  *   outside [-1, E_global), a masked expert with more than max_m rows, a wait
- *   that timed out inside a kernel) set a sticky status word in the
- *   workspace; the offending item is skipped and the call still returns
- *   MOE_OK.  Read the word with moe_read_device_status().
+ *   that timed out inside a kernel) set a status word in the workspace; the
+ *   offending item is skipped and the call still returns MOE_OK.  The word
+ *   holds the first such error since the last moe_plan_layout (which clears
+ *   it) and is read with moe_read_device_status().
  * - Sizes are int64; the weights of the large shapes exceed 2^31 elements.
  */
 #ifndef MOE_GB300_H
@@ -138,13 +139,15 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
                             const void* w2, const uint8_t* w2_sf, moe_ctx** out);
 void moe_ctx_destroy(moe_ctx* ctx);
 
-/* Workspace the caller must provide to the hot calls (device, 1024-byte
- * aligned, at least total_bytes).  No initialisation is needed. */
+/* Workspace the caller must provide to the hot calls (device, 256-byte
+ * aligned, at least total_bytes).  No initialisation is needed: every
+ * region is written before it is read within one pass of the layer. */
 moe_status_t moe_workspace_layout(const moe_ctx* ctx, moe_ws_layout_t* out);
 moe_status_t moe_workspace_size(const moe_ctx* ctx, size_t* bytes);
 
 /* Step 1 [P1 "实现拆解" 2-3, "关键源码片段" ep_moe_kernels.py; P3 "实现拆解" 1]:
- * topk_ids int32 [T, topk] (device; -1 = no assignment).  Writes counts,
+ * topk_ids int32 [T, topk] (device; -1 = no assignment).  Clears the status
+ * word, then writes counts,
  * padded/start/m_indices (compact) or masked_m (masked), src2dst and the
  * 128-row block table into ws.  Inside an expert, assignments keep their
  * flattened t * topk + j order; rows without a token have m_indices -1. */

@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
 int plan_launches() { return 3; }
 
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s) {
+  // the status word reports the first data error of this pass through the layer
+  cudaError_t e = cudaMemsetAsync(p.status, 0, 16, s);
+  if (e != cudaSuccess) return e;
   if (p.chunks > 0) {
     plan_count_rank<<<p.chunks, kPlanChunk, 8 * p.E_local * sizeof(int32_t), s>>>(p);
   }

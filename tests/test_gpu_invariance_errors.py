@@ -117,10 +117,14 @@ def test_host_side_errors():
     p = Problem(T=16, K=256, I=128, E_global=8, E_local=8, topk=2, dtype="fp8", layout="compact",
                 weight_device="cuda")
     good = M.make_shape(16, 256, 128, 8, 8, 2, "fp8", "compact")
-    with pytest.raises(M.MoeError) as e:
-        M.moe_ctx_create(M.make_shape(16, 200, 128, 8, 8, 2, "fp8"), p.w13, p.w13_sf, p.w2, p.w2_sf)
-    assert e.value.code == M.STATUS["MOE_ERR_UNSUPPORTED"]
     handle = ctypes.c_void_p()
+    bad_k = M.make_shape(16, 200, 128, 8, 8, 2, "fp8", "compact")
+    code = M._lib.moe_ctx_create(ctypes.byref(bad_k), p.w13.data_ptr(), p.w13_sf.data_ptr(), p.w2.data_ptr(),
+                                 p.w2_sf.data_ptr(), ctypes.byref(handle))
+    assert code == M.STATUS["MOE_ERR_UNSUPPORTED"]
+    bad_align = M._lib.moe_ctx_create(ctypes.byref(good), p.w13.data_ptr() + 8, p.w13_sf.data_ptr(),
+                                      p.w2.data_ptr(), p.w2_sf.data_ptr(), ctypes.byref(handle))
+    assert bad_align == M.STATUS["MOE_ERR_MISALIGNED"]
     code = M._lib.moe_ctx_create(ctypes.byref(good), p.w13.data_ptr(), None, p.w2.data_ptr(),
                                  p.w2_sf.data_ptr(), ctypes.byref(handle))
     assert code == M.STATUS["MOE_ERR_DTYPE_MISMATCH"]
