@@ -116,6 +116,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def measured_traffic(workload_name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when the kernel sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(workload_name)
+    if not rec:
+        return None
+    csrc = os.path.join(ROOT, "moe_expert_layer_ep_gb300", "csrc")
+    sha = "-".join(hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()[:16]
+                   for f in ("gemm.cu", "common.cuh"))
+    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256_16"] else None
+
+
 def workload(args):
     w = dict(synth.WORKLOADS[args.workload])
     if args.T:
@@ -330,7 +346,9 @@ def run_ours(args, w, world, rank, local):
     else:
         roof = {"bound": "tensor", "achieved": round(g1_tf, 1), "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": round(g1_tf / tensor_peak, 4)}
-    roof.update({"kernel": "grouped_gemm_kernel<stage 1>", "traffic": None,
+    roof.update({"kernel": "grouped_gemm_kernel<stage 1>",
+                 "traffic": measured_traffic(w["name"]) if not args.T else None,
+                 "algorithmic_bytes": int(wm["g1_bytes"]),
                  "peak_source": peaks["source"] + (" (bf16 x 2 for fp8)" if fp8 else "")})
     layer_roof_ms = 1000.0 * max(wm["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
                                  (wm["flops1"] + wm["flops2"]) / (tensor_peak * 1e12))
