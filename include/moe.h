@@ -153,6 +153,38 @@ moe_status_t moe_workspace_size(const moe_ctx* ctx, size_t* bytes);
  * flattened t * topk + j order; rows without a token have m_indices -1. */
 moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, void* stream);
 
+/* Caller-owned outputs of moe_plan_layout_noalloc (device pointers, int32,
+ * same contents as the workspace regions of the same name).  all_tokens =
+ * moe_compact_all_tokens(T * topk, E_local, 128); blocks = all_tokens / 128
+ * (compact) or E_local * ceil(max_m / 128) (masked). */
+typedef struct {
+  int32_t* status;     /* [4]; cleared, then first data error of the call */
+  int32_t* meta;       /* [8]; [0] padded rows, [1] valid 128-row blocks */
+  int32_t* counts;     /* [E_local] */
+  int32_t* padded;     /* [E_local], compact only (NULL allowed for masked) */
+  int32_t* start;      /* [E_local], compact only */
+  int32_t* masked_m;   /* [E_local], masked only (NULL allowed for compact) */
+  int32_t* m_indices;  /* [all_tokens], compact only */
+  int32_t* src2dst;    /* [T * topk] */
+  int32_t* block_info; /* [4 * blocks], 16-byte aligned */
+} moe_plan_outputs_t;
+
+/* No counterpart in the PR reports: a variant of moe_plan_layout for callers
+ * that cannot allocate device memory (for example code inside a framework
+ * whose memory planner owns the device heap and hands it only the tensors it
+ * reads and writes).  It needs no context and no workspace: the caller passes
+ * the shape, topk_ids and the output buffers above, and the plan's scratch
+ * lives in a 1 MiB array inside the library's device image (held by every
+ * GPU that loads the library until the process exits).  Limit:
+ * ceil(T * topk / 256) * E_local + T * topk <= 262144 (for example
+ * T * topk = 65536 with 256 local experts); larger problems return
+ * MOE_ERR_BUFFER_TOO_SMALL.  Allocates nothing (no cudaMalloc/cudaFree or
+ * allocating library call).  The first call on a device looks up the
+ * array's device address; make it before any stream capture.  Calls share
+ * the array: calls that overlap on the GPU race on it. */
+moe_status_t moe_plan_layout_noalloc(const moe_shape_t* shape, const int32_t* topk_ids,
+                                     const moe_plan_outputs_t* out, void* stream);
+
 /* Step 2 [P1 "实现拆解" 3; P2 "实现拆解" 3]: x bf16 [T, K] (device).  FP8:
  * each 128-column group of a token gets the smallest power-of-two scale 2^s
  * with amax <= 448 * 2^s (s clamped to [-127, 127]; byte s + 127) and every

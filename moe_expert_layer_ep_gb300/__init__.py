@@ -51,6 +51,11 @@ _WS_FIELDS = ["total_bytes", "status", "meta", "counts", "padded", "start", "mas
               "block_info", "chunk_hist", "chunk_rank", "a", "a_sf", "h", "h_sf", "y"]
 
 
+class MoePlanOutputs(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in ("status", "meta", "counts", "padded", "start", "masked_m",
+                                               "m_indices", "src2dst", "block_info")]
+
+
 class MoeWsLayout(ctypes.Structure):
     _fields_ = [(f, ctypes.c_uint64) for f in _WS_FIELDS] + [
         ("rows", ctypes.c_int64), ("all_tokens", ctypes.c_int64), ("blocks", ctypes.c_int64),
@@ -81,6 +86,7 @@ def _load():
         "moe_selftest_wait_timeout": (I32, [VP, I64, VP]),
         "moe_sf_offset": (I64, [I64, I64, I64, I32]),
         "moe_strerror": (ctypes.c_char_p, [I32]),
+        "moe_plan_layout_noalloc": (I32, [P(MoeShape), VP, P(MoePlanOutputs), VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -94,7 +100,7 @@ EXPORTED = ("moe_compact_all_tokens", "moe_choose_layout", "moe_ctx_create", "mo
             "moe_workspace_layout", "moe_workspace_size", "moe_plan_layout", "moe_quant_scatter",
             "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2", "moe_combine", "moe_forward",
             "moe_forward_launches", "moe_read_device_status", "moe_clear_device_status",
-            "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror")
+            "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc")
 
 
 def _check(code, what):
@@ -250,6 +256,16 @@ def moe_selftest_wait_timeout(ws, timeout_ns, stream=None):
 
 def moe_sf_offset(block, group, n_groups, row):
     return int(_lib.moe_sf_offset(block, group, n_groups, row))
+
+
+def moe_plan_layout_noalloc(shape, topk_ids, outputs, stream=None):
+    """outputs: dict of int32 CUDA tensors keyed like MoePlanOutputs's fields
+    (missing keys are passed as NULL)."""
+    if topk_ids is not None:
+        _require_cuda("topk_ids", topk_ids, torch.int32, shape.T * shape.topk)
+    o = MoePlanOutputs(**{k: _ptr(v) for k, v in outputs.items()})
+    _check(_lib.moe_plan_layout_noalloc(ctypes.byref(shape), _ptr(topk_ids), ctypes.byref(o), _stream(stream)),
+           "moe_plan_layout_noalloc")
 
 
 def ws_view(ctx, ws, name):
