@@ -46,7 +46,7 @@ typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,      /* null / misshaped argument */
   MOE_ERR_UNSUPPORTED = 2,      /* valid but not implemented (e.g. K % 128 != 0) */
-  MOE_ERR_BUFFER_TOO_SMALL = 3, /* reserved */
+  MOE_ERR_BUFFER_TOO_SMALL = 3, /* problem larger than a fixed-size buffer (moe_plan_layout_noalloc) */
   MOE_ERR_MISALIGNED = 4,       /* a pointer is not 16-byte aligned */
   MOE_ERR_CUDA = 5,             /* a CUDA runtime / driver call failed */
   MOE_ERR_EXPERT_ID = 6,        /* device: topk id outside [-1, E_global) */
@@ -100,7 +100,7 @@ typedef struct {
   uint64_t m_indices;   /* int32[all_tokens] compact: local expert per row, -1 = no token */
   uint64_t src2dst;     /* int32[T * topk] destination row per assignment, -1 = dropped */
   uint64_t block_info;  /* int32[4 * blocks]: {expert, first row, tma row, valid rows} */
-  uint64_t chunk_hist;  /* int32[chunks * E_local] plan scratch */
+  uint64_t chunk_hist;  /* int32[E_local * chunks] plan scratch */
   uint64_t chunk_rank;  /* int32[T * topk]         plan scratch */
   uint64_t a;           /* [rows, K]  fp8 bytes or bf16: expert inputs */
   uint64_t a_sf;        /* fp8: scale chunks of a (see moe_sf_offset) */

@@ -100,6 +100,18 @@ __device__ __forceinline__ Tile load_tile(const GemmArgs& g, int64_t t) {
   return tl;
 }
 
+// Weight rows of the two 128-row B boxes of a tile.
+template <int kStage>
+__device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, int* r0, int* r1) {
+  if (kStage == 1) {
+    *r0 = tl.nb * 128;
+    *r1 = static_cast<int>(g.n_half) + tl.nb * 128;
+  } else {
+    *r0 = tl.nb * kTileN;
+    *r1 = *r0 + 128;
+  }
+}
+
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
 template <bool kFP8, int kStage>
@@ -154,16 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
+
     for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const Tile tl = load_tile(g, t);
       int r0, r1;
-      if (kStage == 1) {
-        r0 = tl.nb * 128;
-        r1 = static_cast<int>(g.n_half) + tl.nb * 128;
-      } else {
-        r0 = tl.nb * kTileN;
-        r1 = r0 + 128;
-      }
+      tile_b_rows<kStage>(g, tl, &r0, &r1);
       const int a_e = g.masked ? tl.expert : 0;
       uint32_t sg_cache = 0, su_cache = 0;
       for (int kb = 0; kb < k_blocks; ++kb) {

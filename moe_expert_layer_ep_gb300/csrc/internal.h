@@ -30,7 +30,7 @@ struct PlanArgs {
   int32_t* m_indices;
   int32_t* src2dst;
   int32_t* block_info;      // int4 per block
-  int32_t* chunk_hist;      // [chunks, E_local]
+  int32_t* chunk_hist;      // [E_local, chunks]
   int32_t* chunk_rank;      // [A]
 };
 

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kPlanChunk) plan_count_rank(PlanArgs p) {
     int total = 0;
 #pragma unroll
     for (int w = 0; w < 8; ++w) total += s_wcnt[w * E + x];
-    p.chunk_hist[static_cast<int64_t>(blockIdx.x) * E + x] = total;
+    p.chunk_hist[static_cast<int64_t>(x) * p.chunks + blockIdx.x] = total;  // [E][chunks]
   }
 }
 
@@ -93,17 +93,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 
 __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
   __shared__ int s_warp[32];
+  __shared__ int s_count[kMaxLocalExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // one warp per expert: exclusive scan of the expert's chunk counts (which
+  // become each chunk's offset inside the expert) and the expert total
+  for (int ex = warp; ex < p.E_local; ex += 32) {
+    int32_t* row = p.chunk_hist + static_cast<int64_t>(ex) * p.chunks;
+    int carry = 0;
+    for (int c0 = 0; c0 < p.chunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < p.chunks ? row[c] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c < p.chunks) row[c] = carry + x - v;
+      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) s_count[ex] = carry;
+  }
+  __syncthreads();
   const int e = threadIdx.x;
   const bool act = e < p.E_local;
-  int count = 0;
-  if (act) {
-    for (int c = 0; c < p.chunks; ++c) {
-      int32_t* cell = p.chunk_hist + static_cast<int64_t>(c) * p.E_local + e;
-      const int v = *cell;
-      *cell = count;  // becomes the chunk's exclusive offset inside expert e
-      count += v;
-    }
-  }
+  const int count = act ? s_count[e] : 0;
   int rows, nblk;
   if (!p.masked) {
     rows = (count + kBlockM - 1) / kBlockM * kBlockM;
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
     const int e = local_expert(p.topk_ids[i], p.E_global, p.E_local, p.expert_start, &bad);
     int32_t dst = -1;
     if (e >= 0) {
-      const int rank = p.chunk_hist[(i / kPlanChunk) * E + e] + p.chunk_rank[i];
+      const int rank = p.chunk_hist[static_cast<int64_t>(e) * p.chunks + i / kPlanChunk] + p.chunk_rank[i];
       if (!p.masked) {
         dst = s_tab[e] + rank;
       } else if (rank < p.max_m) {

@@ -116,7 +116,7 @@ extern "C" moe_status_t moe_plan_layout_noalloc(const moe_shape_t* s, const int3
   p.m_indices = out->m_indices;
   p.src2dst = out->src2dst;
   p.block_info = out->block_info;
-  p.chunk_hist = scratch;                           // [chunks, E_local]
+  p.chunk_hist = scratch;                           // [E_local, chunks]
   p.chunk_rank = scratch + chunks * s->E_local;     // [A]
   return moe::launch_plan(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

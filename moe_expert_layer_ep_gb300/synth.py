@@ -126,6 +126,10 @@ WORKLOADS = {
                          dtype="bf16", layout="compact", zipf_s=None, seed=0x4D6F45_0002),
     "fp8_prefill_zipf": dict(T=8192, K=7168, I=2048, E_global=256, E_local=256, expert_start=0, topk=8,
                              dtype="fp8", layout="compact", zipf_s=1.2, seed=0x4D6F45_0003),
+    # profiling-sized FP8 prefill (1.4 GB of weights): same per-tile shape as
+    # the large prefill, small enough for a full ncu capture
+    "fp8_prefill_e32": dict(T=2048, K=7168, I=2048, E_global=32, E_local=32, expert_start=0, topk=8,
+                            dtype="fp8", layout="compact", zipf_s=None, seed=0x4D6F45_0004),
     "fp8_masked_decode": dict(T=64, K=7168, I=2048, E_global=256, E_local=32, expert_start=0, topk=8,
                               dtype="fp8", layout="masked", zipf_s=None, seed=0x4D6F45_0003),
 }

@@ -124,3 +124,54 @@ def test_hand_computed_permutation_experts():
             if ids[t, j] >= 0:
                 acc += float(wts[t, j]) * expert(x[t], ids[t, j], consts[ids[t, j]])
         assert np.array_equal(out[t], F.bf16_round(acc)), t
+
+
+def test_dequant_fp8_weights_brute_force():
+    """Each element is its E4M3 value times 2^(block exponent) of the 128x128
+    block it sits in; checked element by element with plain loops."""
+    import math
+    rng = np.random.default_rng(6)
+    E, N, C = 1, 256, 384
+    wb = rng.integers(0, 256, size=(E, N, C), dtype=np.uint8)
+    wb[(wb & 0x7F) == 0x7F] = 0x38                          # no NaN codes
+    we = rng.integers(-20, 20, size=(E, N // 128, C // 128))
+    got = oracle.dequant_fp8_weights(wb, we)
+    for n in range(0, N, 7):
+        for c in range(0, C, 5):
+            b = int(wb[0, n, c])
+            sign = -1.0 if b & 0x80 else 1.0
+            ef, mf = (b >> 3) & 0xF, b & 7
+            v = sign * (mf / 8 * 2.0 ** -6 if ef == 0 else (1 + mf / 8) * 2.0 ** (ef - 7))
+            assert got[0, n, c] == v * math.ldexp(1.0, int(we[0, n // 128, c // 128])), (n, c)
+
+
+@pytest.mark.parametrize("mistake", ["swap_gate_up", "transpose_w2", "drop_combine_term"])
+def test_planted_mistakes_are_caught(mistake, monkeypatch):
+    """Plant a plausible mistake in the oracle (CPU only) and check that the
+    hand-computed pin fails with it."""
+    from oracle import moe as om
+    if mistake == "swap_gate_up":
+        def bad(a, w13_e):
+            I = w13_e.shape[0] // 2
+            g, u = a @ w13_e[I:].T, a @ w13_e[:I].T
+            return g, u, om.silu(g) * u
+        monkeypatch.setattr(om, "gemm1_act", bad)
+    elif mistake == "transpose_w2":
+        monkeypatch.setattr(om, "gemm2", lambda h_in, w2_e: oracle.bf16_round(h_in @ w2_e))
+
+        def bad_ffn(a, w13_e, w2_e, dtype, keep=False):
+            g, u, h = om.gemm1_act(a, w13_e)
+            h_in, st = om.store_act(h, dtype)
+            y = oracle.bf16_round(h_in @ w2_e)
+            return (y, {"g": g, "u": u, "h": h, "h_in": h_in, "h_stored": st, "y_acc": h_in @ w2_e}) if keep else y
+        monkeypatch.setattr(om, "expert_ffn", bad_ffn)
+    else:
+        real = om.combine
+
+        def bad(y, src2dst, w):
+            s = src2dst.copy()
+            s[:, -1] = -1
+            return real(y, s, w)
+        monkeypatch.setattr(om, "combine", bad)
+    with pytest.raises(AssertionError):
+        test_hand_computed_permutation_experts()
