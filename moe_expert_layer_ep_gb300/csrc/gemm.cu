@@ -22,13 +22,15 @@
 // its 1x128 UE8M0 quantisation without leaving the CTA.  Stage 2's B tile is
 // 256 consecutive rows of w2.
 //
-// One persistent CTA per SM, 6 warps:
+// One persistent CTA per SM, 10 warps:
 //   warp 0      TMA producer (A tile, B tiles, activation scale chunk; weight
 //               scales expanded into shared memory)
 //   warp 1      TMEM allocation + single-thread MMA issue (tcgen05.cp of the
 //               scale tiles, 4 MMAs of K=32 bytes per 128-byte K block)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (lane quadrant =
-//               warp % 4), activation / quantisation, stores of valid rows
+//   warps 2-9   epilogue, two warps per accumulator lane quadrant (warp % 4),
+//               each with half of the columns: tcgen05.ld, release of the
+//               accumulator, then activation / quantisation and stores of
+//               valid rows
 // A 4-stage mbarrier ring connects producer and MMA; accumulator barriers
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
 // path, whose other tensor-memory columns hold the scale tiles).
@@ -45,7 +47,14 @@ namespace moe {
 namespace {
 
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+// Epilogue warps per (dtype, stage).  The FP8 GEMM1 epilogue (one
+// accumulator: its other tensor-memory columns hold the scale tiles) uses 8,
+// two per accumulator lane quadrant with half of the columns each, copies the
+// accumulator out and releases it before the activation and quantisation.
+// The others use 4 warps that interleave tensor-memory loads and stores
+// chunk by chunk (measured faster there).
+__host__ __device__ constexpr int epi_warps(bool fp8, int stage) { return (fp8 && stage == 1) ? 8 : 4; }
+__host__ __device__ constexpr int threads_for(bool fp8, int stage) { return 64 + 32 * epi_warps(fp8, stage); }
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kKBlockBytes = 128;                  // one 128-byte swizzle atom of K per stage
@@ -58,10 +67,11 @@ constexpr int kOffB = kOffA + kStages * kABytes;
 constexpr int kOffSfa = kOffB + kStages * kBBytes;
 constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
 constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 4;   // ... + per-quadrant amax exchange
 constexpr int kOffHolder = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffHolder + 8;
-constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
+constexpr int kSmemUsed = kOffAmax + 2 * 4 * 2 * 32 * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;       // slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;               // FP8: scale tiles live in columns 256..383
@@ -115,7 +125,7 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
 template <bool kFP8, int kStage>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
@@ -127,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = bars + 2 * kStages;
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint64_t* done = bars + 2 * kStages + 4;
+  uint64_t* xchg = bars + 2 * kStages + 5;  // [4]: the two epilogue warps of a lane quadrant
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kOffHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
@@ -139,9 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage));
     }
     mbar_init(done, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&xchg[q], 64);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
@@ -299,8 +311,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ epilogue
+    // Eight warps: two per tensor-memory lane quadrant (warp % 4), each
+    // owning half of the tile's columns.  A thread copies its accumulator
+    // slice to registers and releases the accumulator before any math, so
+    // the next tile's MMAs never wait on activation, quantisation or stores.
+    constexpr int kEpiWarps = epi_warps(kFP8, kStage);
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;  // 0 when there are four epilogue warps
     const int r = quad * 32 + lane;
+    float* s_amax = reinterpret_cast<float*>(smem + kOffAmax);  // [2 parities][4 quads][2 halves][32]
     int iter = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++iter) {
       const Tile tl = load_tile(g, t);
@@ -318,29 +337,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kTileN) + (static_cast<uint32_t>(quad * 32) << 16);
       const bool row_ok = r < tl.valid;
       const int64_t row = tl.row0 + r;
-      if (kStage == 1) {
-        if (kFP8) {
-          float h[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t gv[32], uv[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, gv);
-            tmem_ld_32x32b_x32(taddr + 128 + c * 32, uv);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) h[c * 32 + i] = silu_mul(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
+      if (kStage == 1 && kEpiWarps == 4) {
+        uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t gv[32], uv[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, gv);
+          tmem_ld_32x32b_x32(taddr + 128 + c * 32, uv);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
           }
-          tc_fence_before();
-          mbar_arrive(&tempty[acc]);
           if (row_ok) {
-            float amax = 0.0f;
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int i = 0; i < 128; ++i) amax = fmaxf(amax, fabsf(h[i]));
+            for (int v = 0; v < 4; ++v) {
+              const int b = v * 8;
+              float hv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) hv[i] = silu_mul(__uint_as_float(gv[b + i]), __uint_as_float(uv[b + i]));
+              d4[v] = make_uint4(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]), pack_bf16x2(hv[4], hv[5]),
+                                 pack_bf16x2(hv[6], hv[7]));
+            }
+          }
+        }
+      } else if (kStage == 1) {
+        // gate columns [64 * half, +64) and the matching up columns 128 later
+        uint32_t g0[32], g1[32], u0[32], u1[32];
+        const uint32_t c0 = static_cast<uint32_t>(64 * half);
+        tmem_ld_32x32b_x32(taddr + c0, g0);
+        tmem_ld_32x32b_x32(taddr + c0 + 32, g1);
+        tmem_ld_32x32b_x32(taddr + 128 + c0, u0);
+        tmem_ld_32x32b_x32(taddr + 128 + c0 + 32, u1);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        float h[64];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          h[i] = silu_mul(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
+          h[32 + i] = silu_mul(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
+        }
+        if (kFP8) {
+          // 1x128 group = this thread's 64 columns + the partner warp's 64
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) amax = fmaxf(amax, fabsf(h[i]));
+          float* slot = s_amax + (((iter & 1) * 4 + quad) * 2) * 32;
+          slot[half * 32 + lane] = amax;
+          mbar_arrive(&xchg[quad]);
+          if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&xchg[quad], iter & 1, abort_flag, g.timeout_ns))) {
+            set_status(g.status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          amax = fmaxf(amax, slot[(half ^ 1) * 32 + lane]);
+          if (row_ok) {
             const int s = ue8m0_exponent(amax);
             const float mul = exp2_neg(s);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + row * g.out_ld + tl.nb * 128);
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) + row * g.out_ld + tl.nb * 128 + 64 * half);
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
+            for (int v = 0; v < 4; ++v) {
               uint4 o;
               const int b = v * 16;
               o.x = cvt_e4m3x2(h[b + 0] * mul, h[b + 1] * mul) | (cvt_e4m3x2(h[b + 2] * mul, h[b + 3] * mul) << 16);
@@ -350,38 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (cvt_e4m3x2(h[b + 14] * mul, h[b + 15] * mul) << 16);
               dst[v] = o;
             }
-            *reinterpret_cast<uint32_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
-                                         sf_row_offset(r)) = static_cast<uint32_t>(s + 127) * 0x01010101u;
+            if (half == 0) {
+              *reinterpret_cast<uint32_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
+                                           sf_row_offset(r)) = static_cast<uint32_t>(s + 127) * 0x01010101u;
+            }
           }
-        } else {
-          uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128;
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t gv[32], uv[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, gv);
-            tmem_ld_32x32b_x32(taddr + 128 + c * 32, uv);
-            tmem_ld_wait();
-            if (c == 3) {
-              tc_fence_before();
-              mbar_arrive(&tempty[acc]);
-            }
-            if (row_ok) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        } else if (row_ok) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128 + 64 * half);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const int b = v * 8;
-                uint4 o;
-                o.x = pack_bf16x2(silu_mul(__uint_as_float(gv[b + 0]), __uint_as_float(uv[b + 0])),
-                                  silu_mul(__uint_as_float(gv[b + 1]), __uint_as_float(uv[b + 1])));
-                o.y = pack_bf16x2(silu_mul(__uint_as_float(gv[b + 2]), __uint_as_float(uv[b + 2])),
-                                  silu_mul(__uint_as_float(gv[b + 3]), __uint_as_float(uv[b + 3])));
-                o.z = pack_bf16x2(silu_mul(__uint_as_float(gv[b + 4]), __uint_as_float(uv[b + 4])),
-                                  silu_mul(__uint_as_float(gv[b + 5]), __uint_as_float(uv[b + 5])));
-                o.w = pack_bf16x2(silu_mul(__uint_as_float(gv[b + 6]), __uint_as_float(uv[b + 6])),
-                                  silu_mul(__uint_as_float(gv[b + 7]), __uint_as_float(uv[b + 7])));
-                d4[v] = o;
-              }
-            }
+          for (int v = 0; v < 8; ++v) {
+            const int b = v * 8;
+            dst[v] = make_uint4(pack_bf16x2(h[b + 0], h[b + 1]), pack_bf16x2(h[b + 2], h[b + 3]),
+                                pack_bf16x2(h[b + 4], h[b + 5]), pack_bf16x2(h[b + 6], h[b + 7]));
           }
         }
       } else {
@@ -430,7 +470,7 @@ cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kStage><<<grid, kThreads, kSmemBytes, s>>>(a, b, g);
+  grouped_gemm_kernel<kFP8, kStage><<<grid, threads_for(kFP8, kStage), kSmemBytes, s>>>(a, b, g);
   return cudaGetLastError();
 }
 
