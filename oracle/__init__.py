@@ -23,6 +23,8 @@ Pinning status (what each function is checked against in ``tests/``):
 * ``layout``: the static compact bound against brute force over every
   routing of tiny problems; plan invariants (bijection, stability, ``-1``
   padding) on random routings.
+* ``requant``: an element-by-element restatement with torch's casts and a
+  brute-force exponent search; exact round trip for power-of-two scales.
 * ``moe``: layout-based forward == per-token loop (bitwise); k=1 single expert
   == a textbook SwiGLU MLP in torch float64; hand-computed small-integer
   weights; masked == compact (bitwise).
@@ -56,3 +58,4 @@ from .moe import (  # noqa: F401
     forward_per_token,
     silu,
 )
+from .requant import requant_block_ue8m0  # noqa: F401
