@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="layer", choices=["layer", "requant"],
+                    help="layer: the MoE layer step (default); requant: load-time UE8M0 weight requantisation")
     return ap.parse_args()
 
 
@@ -410,6 +412,43 @@ def run_ours(args, w, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_requant(args, w, local):
+    """Time moe_requant_weights_ue8m0 on the workload's w13 shape (load-time
+    weight preparation; HBM-bound: reads and writes each weight byte once)."""
+    import moe_expert_layer_ep_gb300 as M
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    E, N, C = w["E_local"], 2 * w["I"], w["K"]
+    g = torch.Generator(device=dev).manual_seed(w["seed"])
+    win = torch.randint(0, 126, (E, N, C), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
+    sin = torch.rand((E, N // 128, C // 128), generator=g, device=dev) * 2.0 ** -12 + 2.0 ** -13
+    wout = torch.empty_like(win)
+    sout = torch.empty((E, N // 128, C // 128), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        M.moe_requant_weights_ue8m0(win, sin, wout, sout)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0.record()
+        for _ in range(args.steps):
+            M.moe_requant_weights_ue8m0(win, sin, wout, sout)
+        t1.record()
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    nbytes = 2 * win.numel() + sin.numel() * 4 + sout.numel()
+    peaks = load_peaks()
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    print(json.dumps({"metric": "load-time UE8M0 weight requantisation bandwidth", "value": round(gbs, 1),
+                      "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": "e4m3+fp32->e4m3+ue8m0",
+                      "data": "synthetic", "config": {"workload": w["name"] + ":w13", "shape": [E, N, C]},
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                   "kernel": "requant_kernel", "traffic": None},
+                      "clocks": clk.summary(), "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -419,6 +458,10 @@ def main():
         backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
         torch.distributed.init_process_group(backend=backend)
     try:
+        if args.op == "requant":
+            if rank == 0:
+                run_requant(args, w, local)
+            return
         if args.impl == "reference":
             run_reference(args, w, world, rank)
         else:

@@ -216,6 +216,19 @@ moe_status_t moe_combine(moe_ctx* ctx, const float* topk_weights, const void* ws
 moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids,
                          const float* topk_weights, void* ws, void* out_bf16, void* stream);
 
+/* Weight preparation, run once at load time [P1 "实现拆解" 1, "关键源码片段"
+ * fp8.py: both expert weight tensors are requantised with UE8M0 block scales
+ * through a bfloat16 intermediate].  w_in: e4m3 bytes [E, N, C]; scale_in:
+ * fp32 [E, N/128, C/128], the dequantisation multiplier of each 128x128
+ * block.  Per block: v = bf16(fp32(q) * s); e = smallest integer with
+ * amax|v| <= 448 * 2^e (clamped to [-127, 127]); q' = e4m3(v * 2^-e), round to
+ * nearest even, saturating.  Writes w_out [E, N, C] and the UE8M0 bytes e + 127
+ * to scale_out [E, N/128, C/128] -- the weight format moe_ctx_create takes.
+ * w_out may equal w_in.  N and C must be multiples of 128; inputs must be
+ * finite.  Device pointers; enqueued on stream. */
+moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_in, uint8_t* w_out,
+                                       uint8_t* scale_out, int64_t E, int64_t N, int64_t C, void* stream);
+
 /* Number of kernel launches one moe_forward enqueues (for launch accounting). */
 int32_t moe_forward_launches(const moe_ctx* ctx);
 

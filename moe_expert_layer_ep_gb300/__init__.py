@@ -87,6 +87,7 @@ def _load():
         "moe_sf_offset": (I64, [I64, I64, I64, I32]),
         "moe_strerror": (ctypes.c_char_p, [I32]),
         "moe_plan_layout_noalloc": (I32, [P(MoeShape), VP, P(MoePlanOutputs), VP]),
+        "moe_requant_weights_ue8m0": (I32, [VP, VP, VP, VP, I64, I64, I64, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -100,7 +101,8 @@ EXPORTED = ("moe_compact_all_tokens", "moe_choose_layout", "moe_ctx_create", "mo
             "moe_workspace_layout", "moe_workspace_size", "moe_plan_layout", "moe_quant_scatter",
             "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2", "moe_combine", "moe_forward",
             "moe_forward_launches", "moe_read_device_status", "moe_clear_device_status",
-            "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc")
+            "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc",
+            "moe_requant_weights_ue8m0")
 
 
 def _check(code, what):
@@ -266,6 +268,23 @@ def moe_plan_layout_noalloc(shape, topk_ids, outputs, stream=None):
     o = MoePlanOutputs(**{k: _ptr(v) for k, v in outputs.items()})
     _check(_lib.moe_plan_layout_noalloc(ctypes.byref(shape), _ptr(topk_ids), ctypes.byref(o), _stream(stream)),
            "moe_plan_layout_noalloc")
+
+
+def moe_requant_weights_ue8m0(w_in, scale_in, w_out=None, scale_out=None, stream=None):
+    """w_in uint8 [E, N, C] e4m3; scale_in float32 [E, N/128, C/128].  Returns
+    (w_out, scale_out) with UE8M0 block scales (see include/moe.h)."""
+    E, N, C = w_in.shape
+    _require_cuda("w_in", w_in, torch.uint8)
+    _require_cuda("scale_in", scale_in, torch.float32, E * (N // 128) * (C // 128))
+    if w_out is None:
+        w_out = torch.empty_like(w_in)
+    if scale_out is None:
+        scale_out = torch.empty((E, N // 128, C // 128), dtype=torch.uint8, device=w_in.device)
+    _require_cuda("w_out", w_out, torch.uint8, w_in.numel())
+    _require_cuda("scale_out", scale_out, torch.uint8, E * (N // 128) * (C // 128))
+    _check(_lib.moe_requant_weights_ue8m0(_ptr(w_in), _ptr(scale_in), _ptr(w_out), _ptr(scale_out), E, N, C,
+                                          _stream(stream)), "moe_requant_weights_ue8m0")
+    return w_out, scale_out
 
 
 def ws_view(ctx, ws, name):

@@ -398,6 +398,16 @@ moe_status_t moe_selftest_wait_timeout(void* ws, int64_t timeout_ns, void* strea
                                                static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_in, uint8_t* w_out,
+                                       uint8_t* scale_out, int64_t E, int64_t N, int64_t C, void* stream) {
+  if (E < 0 || N < 0 || C < 0) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || C % 128) return MOE_ERR_UNSUPPORTED;
+  if (E * N * C == 0) return MOE_OK;
+  if (!w_in || !scale_in || !w_out || !scale_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_in) || !aligned16(w_out) || (reinterpret_cast<uintptr_t>(scale_in) & 3u)) return MOE_ERR_MISALIGNED;
+  return cuda_status(moe::launch_requant(w_in, scale_in, w_out, scale_out, E, N, C, static_cast<cudaStream_t>(stream)));
+}
+
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {
   return moe::sf_chunk_offset(block, group, n_groups) + moe::sf_row_offset(row);
 }

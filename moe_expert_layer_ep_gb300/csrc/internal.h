@@ -85,6 +85,8 @@ cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUtensorMap& map_b, int grid,
                         cudaStream_t s);
+cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
+                           int64_t N, int64_t C, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 int plan_launches();

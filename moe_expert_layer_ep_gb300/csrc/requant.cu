@@ -1,0 +1,94 @@
+// moe_requant_weights_ue8m0: load-time requantisation of 128x128
+// block-scaled FP8 weights to power-of-two (UE8M0) block scales.
+//
+// "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
+// "实现拆解" step 1 and "关键源码片段" fp8.py: both expert weight tensors of
+// a standard MoE layer are requantised with UE8M0 block scales for the
+// grouped GEMMs, through a bfloat16 intermediate.  Per 128x128 block:
+//   v  = bf16(fp32(q) * s)                 (s: the block's fp32 scale)
+//   e  = smallest integer with amax|v| <= 448 * 2^e, clamped to [-127, 127]
+//   q' = e4m3(v * 2^-e)                    (round to nearest even, saturating)
+// One CTA per block: 512 threads, 32 bytes (a quarter row) each, read once,
+// reduced, written once; in-place operation (w_out == w_in) is allowed
+// because a CTA reads its whole block before writing it.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRequantThreads = 512;
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+__global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* w_in, const float* s_in,
+                                                                 uint8_t* w_out, uint8_t* s_out, int64_t N,
+                                                                 int64_t C) {
+  __shared__ float s_red[kRequantThreads / 32];
+  const int64_t nbn = N / 128, nbc = C / 128;
+  const int64_t blk = blockIdx.x;
+  const int64_t e = blk / (nbn * nbc);
+  const int64_t rb = (blk / nbc) % nbn;
+  const int64_t cb = blk % nbc;
+  const float scale = s_in[blk];
+  const int tid = threadIdx.x;
+  const int64_t row = rb * 128 + (tid >> 2);
+  const int64_t off = (e * N + row) * C + cb * 128 + (tid & 3) * 32;
+
+  // the bf16 intermediate, kept packed two values per register
+  uint32_t vp[16];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(w_in + off + 16 * i);
+    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+      for (int b = 0; b < 4; b += 2) {
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_to_float((words[w] >> (8 * b)) & 0xFFu) * scale,
+                                                        e4m3_to_float((words[w] >> (8 * b + 8)) & 0xFFu) * scale);
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(&pr);
+        vp[i * 8 + w * 2 + b / 2] = u;
+        const float2 f = unpack_bf16x2(u);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  if ((tid & 31) == 0) s_red[tid >> 5] = amax;
+  __syncthreads();
+  amax = s_red[0];
+#pragma unroll
+  for (int i = 1; i < kRequantThreads / 32; ++i) amax = fmaxf(amax, s_red[i]);
+  const int s = ue8m0_exponent(amax);
+  const float mul = exp2_neg(s);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t outw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 lo = unpack_bf16x2(vp[i * 8 + w * 2]), hi = unpack_bf16x2(vp[i * 8 + w * 2 + 1]);
+      outw[w] = cvt_e4m3x2(lo.x * mul, lo.y * mul) | (cvt_e4m3x2(hi.x * mul, hi.y * mul) << 16);
+    }
+    *reinterpret_cast<uint4*>(w_out + off + 16 * i) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  }
+  if (tid == 0) s_out[blk] = static_cast<uint8_t>(s + 127);
+}
+
+}  // namespace
+
+cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
+                           int64_t N, int64_t C, cudaStream_t st) {
+  const int64_t blocks = E * (N / 128) * (C / 128);
+  if (blocks <= 0) return cudaSuccess;
+  requant_kernel<<<static_cast<unsigned>(blocks), kRequantThreads, 0, st>>>(w_in, s_in, w_out, s_out, N, C);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
