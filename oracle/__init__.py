@@ -23,6 +23,9 @@ Pinning status (what each function is checked against in ``tests/``):
 * ``layout``: the static compact bound against brute force over every
   routing of tiny problems; plan invariants (bijection, stability, ``-1``
   padding) on random routings.
+* ``router``: selection against a keyed sort and brute force over tiny rows
+  with ties; softmax against scipy's and torch's; logits against torch
+  float64.
 * ``requant``: an element-by-element restatement with torch's casts and a
   brute-force exponent search; exact round trip for power-of-two scales.
 * ``moe``: layout-based forward == per-token loop (bitwise); k=1 single expert
@@ -59,3 +62,4 @@ from .moe import (  # noqa: F401
     silu,
 )
 from .requant import requant_block_ue8m0  # noqa: F401
+from . import router  # noqa: F401
