@@ -42,8 +42,9 @@ def parse():
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="layer", choices=["layer", "requant"],
-                    help="layer: the MoE layer step (default); requant: load-time UE8M0 weight requantisation")
+    ap.add_argument("--op", default="layer", choices=["layer", "requant", "router"],
+                    help="layer: the MoE layer step (default); requant: load-time UE8M0 weight requantisation; "
+                         "router: the fp32 router (logits + top-k + softmax) on the workload's tokens")
     return ap.parse_args()
 
 
@@ -449,6 +450,90 @@ def run_requant(args, w, local):
                       "clocks": clk.summary(), "gpu_launches": args.steps}), flush=True)
 
 
+def run_router(args, w, local):
+    """Time moe_route (fp32 router logits + top-k + softmax) on the workload's
+    tokens.  Each timed call is preceded by a 256 MB write that evicts L2 (the
+    router weights alone would stay cached), and the calls are replayed from
+    one CUDA graph with events around each call only, as a decode step runs
+    them.  The bound is whichever of the fp32 FMA peak (SMs x 128 lanes x 2
+    flops x clock) and the measured HBM copy bandwidth gives the longer time
+    for the call's flops and bytes."""
+    import moe_expert_layer_ep_gb300 as M
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    T, K, E, k = w["T"], w["K"], w["E_global"], w["topk"]
+    x = synth.activations(T, K, w["seed"], dev)
+    g = torch.Generator(device=dev).manual_seed(w["seed"] + 5)
+    wr = torch.randn((E, K), generator=g, device=dev) * 0.02
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        M.moe_route(x, wr, k, logits, ids, wts)
+    torch.cuda.synchronize()
+    timing = "cuda-graph replay"
+    try:
+        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(args.steps)]
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            M.moe_route(x, wr, k, logits, ids, wts)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for s in range(args.steps):
+                flush.fill_(s & 0xFF)
+                ev[s][0].record()
+                M.moe_route(x, wr, k, logits, ids, wts)
+                ev[s][1].record()
+        graph.replay()
+        torch.cuda.synchronize()
+        run_timed = graph.replay
+    except Exception:
+        timing = "eager launches"
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        stream = torch.cuda.current_stream()
+
+        def run_timed():
+            for s in range(args.steps):
+                flush.fill_(s & 0xFF)
+                ev[s][0].record(stream)
+                M.moe_route(x, wr, k, logits, ids, wts)
+                ev[s][1].record(stream)
+    with ClockSampler(local) as clk:
+        run_timed()
+        torch.cuda.synchronize()
+    per = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
+    ms = float(per.mean())
+    flops = 2.0 * T * K * E
+    nbytes = 4.0 * E * K + 2.0 * T * K + 4.0 * T * E + 8.0 * T * k
+    props = torch.cuda.get_device_properties(dev)
+    clk_s = clk.summary()
+    mhz = clk_s["sm_mhz"] or 2070.0
+    alu_peak = props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+    peaks = load_peaks()
+    sec = ms / 1000.0
+    if flops / (alu_peak * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "alu", "achieved": round(flops / sec / 1e12, 2), "peak": round(alu_peak, 1),
+                "unit": "TFLOP/s", "frac": round(flops / sec / 1e12 / alu_peak, 4),
+                "peak_source": "SMs x 128 fp32 lanes x 2 flops x median SM clock"}
+    else:
+        gbs = nbytes / sec / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peaks["source"]}
+    roof.update({"kernel": "moe_route (router_logits + topk_softmax)", "traffic": None,
+                 "algorithmic_bytes": int(nbytes), "algorithmic_flops": flops})
+    print(json.dumps({"metric": "fp32 router (logits + top-k + softmax) throughput", "value": round(T / sec, 1),
+                      "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+                      "ms_per_step": round(ms, 4),
+                      "ms_p10_p90": [round(float(np.percentile(per, q)), 4) for q in (10, 90)],
+                      "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+                      "config": {"workload": w["name"], "T": T, "K": K, "E": E, "topk": k,
+                                 "l2": "flushed before each call (256 MB write)", "timing": timing},
+                      "roofline": roof, "clocks": clk_s, "gpu_launches": 2 * args.steps}), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -458,9 +543,9 @@ def main():
         backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
         torch.distributed.init_process_group(backend=backend)
     try:
-        if args.op == "requant":
+        if args.op in ("requant", "router"):
             if rank == 0:
-                run_requant(args, w, local)
+                (run_requant if args.op == "requant" else run_router)(args, w, local)
             return
         if args.impl == "reference":
             run_reference(args, w, world, rank)

@@ -229,6 +229,25 @@ moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_i
 moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_in, uint8_t* w_out,
                                        uint8_t* scale_out, int64_t E, int64_t N, int64_t C, void* stream);
 
+/* The router that produces the layer's routing input [P3 "关联脉络": the
+ * MoE router GEMM is kept in fp32 so that expert selection does not flip under
+ * deterministic inference; P1 "关键源码片段" deep_gemm.py: the layer takes
+ * standard top-k ids and weights].
+ *   logits[t, e] = sum_k x[t, k] * w_router[e, k] in fp32 (x bf16 [T, K], exact
+ *     in fp32; w_router fp32 [E_global, K]); every logit sums its K products in
+ *     four chains (k mod 4, ascending k) combined as (c0 + c1) + (c2 + c3),
+ *     whatever T, so a token's results do not depend on its batch;
+ *   topk_ids[t, :] int32 [T, topk]: the topk largest logits in descending
+ *     order, equal logits ordered by the lower expert id;
+ *   topk_weights[t, j] fp32 = exp(z_j - z_0) / sum_i exp(z_i - z_0) over the
+ *     selected logits, the sum taken in j order.
+ * K must be a multiple of 128, E_global <= 1024, topk <= min(64, E_global)
+ * (MOE_ERR_UNSUPPORTED otherwise); all pointers device, 16-byte aligned
+ * (MOE_ERR_MISALIGNED); the caller owns every buffer; enqueued on stream,
+ * graph-capturable.  Inputs must be finite. */
+moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int64_t K, int32_t E_global,
+                       int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
+
 /* Number of kernel launches one moe_forward enqueues (for launch accounting). */
 int32_t moe_forward_launches(const moe_ctx* ctx);
 

@@ -88,6 +88,7 @@ def _load():
         "moe_strerror": (ctypes.c_char_p, [I32]),
         "moe_plan_layout_noalloc": (I32, [P(MoeShape), VP, P(MoePlanOutputs), VP]),
         "moe_requant_weights_ue8m0": (I32, [VP, VP, VP, VP, I64, I64, I64, VP]),
+        "moe_route": (I32, [VP, VP, I64, I64, I32, I32, VP, VP, VP, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -102,7 +103,7 @@ EXPORTED = ("moe_compact_all_tokens", "moe_choose_layout", "moe_ctx_create", "mo
             "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2", "moe_combine", "moe_forward",
             "moe_forward_launches", "moe_read_device_status", "moe_clear_device_status",
             "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc",
-            "moe_requant_weights_ue8m0")
+            "moe_requant_weights_ue8m0", "moe_route")
 
 
 def _check(code, what):
@@ -285,6 +286,28 @@ def moe_requant_weights_ue8m0(w_in, scale_in, w_out=None, scale_out=None, stream
     _check(_lib.moe_requant_weights_ue8m0(_ptr(w_in), _ptr(scale_in), _ptr(w_out), _ptr(scale_out), E, N, C,
                                           _stream(stream)), "moe_requant_weights_ue8m0")
     return w_out, scale_out
+
+
+def moe_route(x, w_router, topk, logits=None, topk_ids=None, topk_weights=None, stream=None):
+    """x bf16 [T, K], w_router fp32 [E, K] -> (topk_ids int32 [T, k],
+    topk_weights fp32 [T, k], logits fp32 [T, E]); see include/moe.h."""
+    T, K = x.shape
+    E = w_router.shape[0]
+    _require_cuda("x", x, torch.bfloat16)
+    _require_cuda("w_router", w_router, torch.float32, E * K)
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    _require_cuda("logits", logits, torch.float32, T * E)
+    _require_cuda("topk_ids", topk_ids, torch.int32, T * topk)
+    _require_cuda("topk_weights", topk_weights, torch.float32, T * topk)
+    _check(_lib.moe_route(_ptr(x), _ptr(w_router), T, K, E, topk, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
+                          _stream(stream)), "moe_route")
+    return topk_ids, topk_weights, logits
 
 
 def ws_view(ctx, ws, name):

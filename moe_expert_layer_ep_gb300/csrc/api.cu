@@ -408,6 +408,20 @@ moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_i
   return cuda_status(moe::launch_requant(w_in, scale_in, w_out, scale_out, E, N, C, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int64_t K, int32_t E_global,
+                       int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* stream) {
+  if (T < 0 || K <= 0 || E_global <= 0 || topk <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 128 || E_global > moe::kMaxRouterExperts || topk > moe::kMaxTopk || topk > E_global)
+    return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x_bf16 || !w_router || !logits || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(w_router) || !aligned16(logits) || !aligned16(topk_ids) ||
+      !aligned16(topk_weights))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(moe::launch_route(x_bf16, w_router, T, K, E_global, topk, logits, topk_ids, topk_weights,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {
   return moe::sf_chunk_offset(block, group, n_groups) + moe::sf_row_offset(row);
 }

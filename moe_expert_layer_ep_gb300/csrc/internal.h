@@ -11,6 +11,8 @@ constexpr int kPlanChunk = 256;   // assignments per plan CTA (8 warps x 32)
 constexpr int kMaxLocalExperts = 1024;
 constexpr int kMaxTopk = 64;
 constexpr int kBlockM = 128;      // rows per expert block == compact block_e
+constexpr int kMaxRouterExperts = 1024;
+constexpr int kRouterSmallBatch = 256;   // router batches up to this size take the small-batch kernel
 
 struct PlanArgs {
   const int32_t* topk_ids;  // [A]
@@ -87,6 +89,8 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUten
                         cudaStream_t s);
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t s);
+cudaError_t launch_route(const void* x, const float* w, int64_t T, int64_t K, int E, int topk, float* logits,
+                         int32_t* ids, float* wts, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 int plan_launches();
