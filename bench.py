@@ -42,9 +42,10 @@ def parse():
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="layer", choices=["layer", "requant", "router"],
+    ap.add_argument("--op", default="layer", choices=["layer", "requant", "router", "crossover"],
                     help="layer: the MoE layer step (default); requant: load-time UE8M0 weight requantisation; "
-                         "router: the fp32 router (logits + top-k + softmax) on the workload's tokens")
+                         "router: the fp32 router (logits + top-k + softmax) on the workload's tokens; "
+                         "crossover: masked vs compact layout across E_local and T")
     return ap.parse_args()
 
 
@@ -534,6 +535,80 @@ def run_router(args, w, local):
                       "roofline": roof, "clocks": clk_s, "gpu_launches": 2 * args.steps}), flush=True)
 
 
+CROSSOVER_E_LOCAL = (8, 16, 32, 64, 128, 256)
+CROSSOVER_T = (1, 16, 64, 256, 1024, 4096)
+
+
+def run_crossover(args, w, local):
+    """Masked vs compact layout: the whole layer, one graph of --steps
+    forwards per point with events between the stages, for every E_local in
+    CROSSOVER_E_LOCAL and T in CROSSOVER_T.  FP8, the workload's K and I,
+    E_global 256 with the rank's experts first (ids outside them are dropped),
+    uniform N(0, 1) router logits, top-8; masked max_m = T rounded up to 16.
+    One JSON line per (E_local, T) with both layouts' stage times."""
+    import moe_expert_layer_ep_gb300 as M
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    K, I, topk, E_g = w["K"], w["I"], 8, 256
+    names = ["plan", "quant_scatter", "gemm_w13_act", "gemm_w2", "combine"]
+    for E_l in CROSSOVER_E_LOCAL:
+        w13, w13s = synth.fp8_expert_weights(E_l, 2 * I, K, w["seed"] + 2, dev)
+        w2, w2s = synth.fp8_expert_weights(E_l, K, I, w["seed"] + 3, dev)
+        for T in CROSSOVER_T:
+            x = synth.activations(T, K, w["seed"], dev)
+            ids_h, wts_h = synth.routing(T, E_g, topk, w["seed"] + 1)
+            ids, wts = ids_h.to(dev), wts_h.to(dev)
+            local_rows = int(((ids_h >= 0) & (ids_h < E_l)).sum())
+            active = int(torch.unique(ids_h[(ids_h >= 0) & (ids_h < E_l)]).numel())
+            res = {}
+            for layout in ("compact", "masked"):
+                max_m = (T + 15) // 16 * 16 if layout == "masked" else 0
+                shape = M.make_shape(T, K, I, E_g, E_l, topk, "fp8", layout, 0, max_m)
+                ctx = M.moe_ctx_create(shape, w13, w13s, w2, w2s)
+                ws = M.alloc_workspace(ctx, dev)
+                out = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+                stages = [lambda: M.moe_plan_layout(ctx, ids, ws), lambda: M.moe_quant_scatter(ctx, x, ws),
+                          lambda: M.moe_grouped_gemm_w13_act(ctx, ws), lambda: M.moe_grouped_gemm_w2(ctx, ws),
+                          lambda: M.moe_combine(ctx, wts, ws, out)]
+                M.moe_clear_device_status(ws)
+                for _ in range(max(args.warmup, 3)):
+                    M.moe_forward(ctx, x, ids, wts, ws, out)
+                torch.cuda.synchronize()
+                ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+                      for _ in range(args.steps)]
+                side = torch.cuda.Stream(device=dev)
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    M.moe_forward(ctx, x, ids, wts, ws, out)
+                torch.cuda.current_stream().wait_stream(side)
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for st in range(args.steps):
+                        ev[st][0].record()
+                        for i, fn in enumerate(stages):
+                            fn()
+                            ev[st][i + 1].record()
+                graph.replay()
+                torch.cuda.synchronize()
+                graph.replay()
+                torch.cuda.synchronize()
+                status = M.moe_read_device_status(ws)
+                if status != 0:
+                    raise RuntimeError(f"device status {status} (E_local {E_l}, T {T}, {layout})")
+                st_ms = np.median(np.array([[ev[s][i].elapsed_time(ev[s][i + 1]) for i in range(5)]
+                                            for s in range(args.steps)]), axis=0)
+                res[layout] = {"ms": round(float(st_ms.sum()), 4),
+                               "stage_ms": {n: round(float(v), 4) for n, v in zip(names, st_ms)},
+                               "ws_mb": round(M.moe_workspace_size(ctx) / 2 ** 20, 1)}
+                del graph, ws, ctx          # the context is destroyed with its last reference
+            print(json.dumps({"op": "crossover", "E_local": E_l, "T": T, "local_rows": local_rows,
+                              "active_experts": active, "auto": "masked" if M.moe_choose_layout(E_g, E_l) == 2
+                              else "compact", "masked_over_compact": round(res["masked"]["ms"] / res["compact"]["ms"], 3),
+                              **res}), flush=True)
+        del w13, w13s, w2, w2s
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -543,9 +618,9 @@ def main():
         backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
         torch.distributed.init_process_group(backend=backend)
     try:
-        if args.op in ("requant", "router"):
+        if args.op in ("requant", "router", "crossover"):
             if rank == 0:
-                (run_requant if args.op == "requant" else run_router)(args, w, local)
+                {"requant": run_requant, "router": run_router, "crossover": run_crossover}[args.op](args, w, local)
             return
         if args.impl == "reference":
             run_reference(args, w, world, rank)
