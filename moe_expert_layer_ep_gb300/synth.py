@@ -93,6 +93,31 @@ def fp8_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
     return w, sf
 
 
+def mxfp8_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
+    """MXFP8 weights for experts first_expert .. first_expert+E-1: one UE8M0
+    exponent per row and 32-column block.
+
+    Returns (w uint8 [E, N, C] E4M3 bytes, w_sf uint8 [E, N, C/32] UE8M0
+    bytes, row-major: the natural MX layout).
+    """
+    assert N % 128 == 0 and C % 128 == 0
+    w = torch.empty((E, N, C), dtype=torch.uint8, device=device)
+    sf = torch.empty((E, N, C // 32), dtype=torch.uint8, device=device)
+    rows_per_chunk = max(128, (1 << 26) // C // 128 * 128)
+    for i in range(E):
+        g = _gen(seed * 1_000_003 + first_expert + i + 7919, device)
+        choice = torch.randint(0, len(FP8_WEIGHT_EXPONENTS), (N, C // 32), generator=g, device=device)
+        exps = torch.tensor(FP8_WEIGHT_EXPONENTS, device=device)[choice]
+        sf[i] = (exps + 127).to(torch.uint8)
+        for r0 in range(0, N, rows_per_chunk):
+            r1 = min(N, r0 + rows_per_chunk)
+            v = torch.randn((r1 - r0, C), generator=g, device=device, dtype=torch.float32) * 0.02
+            mult = torch.exp2(-exps[r0:r1].to(torch.float32))
+            v = (v.view(r1 - r0, C // 32, 32) * mult.view(r1 - r0, C // 32, 1)).clamp_(-448.0, 448.0)
+            w[i, r0:r1] = v.view(r1 - r0, C).to(torch.float8_e4m3fn).view(torch.uint8)
+    return w, sf
+
+
 def bf16_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
     """BF16 weights [E, N, C] ~ N(0, 0.02)."""
     w = torch.empty((E, N, C), dtype=torch.bfloat16, device=device)

@@ -19,7 +19,10 @@ imports the product package; the product path never imports it.
 Pinning status (what each function is checked against in ``tests/``):
 
 * ``formats``: bf16 / e4m3 rounding against torch's own dtype casts over
-  exhaustive bf16 sweeps; UE8M0 exponent against a brute-force search.
+  exhaustive bf16 sweeps; UE8M0 exponent against a brute-force search;
+  1x32 (MXFP8) groups against torch's e4m3 cast with a brute-force minimal
+  exponent, against the 1x128 routine on tiled blocks, and equal to 1x128
+  where the four blocks of a group share their exponent.
 * ``layout``: the static compact bound against brute force over every
   routing of tiny problems; plan invariants (bijection, stability, ``-1``
   padding) on random routings.
@@ -30,7 +33,8 @@ Pinning status (what each function is checked against in ``tests/``):
   brute-force exponent search; exact round trip for power-of-two scales.
 * ``moe``: layout-based forward == per-token loop (bitwise); k=1 single expert
   == a textbook SwiGLU MLP in torch float64; hand-computed small-integer
-  weights; masked == compact (bitwise).
+  weights; masked == compact (bitwise); MXFP8 weight dequantisation element
+  by element with plain loops.
 """
 
 from .formats import (  # noqa: F401
@@ -44,6 +48,9 @@ from .formats import (  # noqa: F401
     ue8m0_exponent,
     quant_fp8_1x128,
     dequant_1x128,
+    quant_fp8_groups,
+    dequant_groups,
+    quant_mxfp8_1x32,
 )
 from .layout import (  # noqa: F401
     compact_all_tokens,
@@ -53,6 +60,7 @@ from .layout import (  # noqa: F401
 from .moe import (  # noqa: F401
     combine,
     dequant_fp8_weights,
+    dequant_mx_weights,
     expert_ffn,
     gemm1_act,
     gemm2,

@@ -16,6 +16,11 @@ error).  Reading adopted where the report is silent: for each 128-column
 group the exponent is the smallest integer s with amax <= 448 * 2^s, clamped
 to [-127, 127] (s = -127 when amax == 0), and every element is divided by
 that final scale before rounding to E4M3.
+
+MXFP8 (the 1x32 variant, which the standard-dispatch report lists as not yet
+covered, section "风险与影响" item 5) is read as the same element format and
+the same exponent rule over 32-column blocks (the OCP microscaling block
+size), for activations, the GEMM1 output and each weight row.
 """
 
 import math
@@ -98,28 +103,47 @@ def ue8m0_exponent(amax):
     return np.clip(s, -127, 127).astype(np.int64)
 
 
-def quant_fp8_1x128(x):
-    """Per-row, per-128-column FP8 quantisation with UE8M0 scales.
+def quant_fp8_groups(x, group):
+    """Per-row FP8 quantisation with one UE8M0 scale per ``group`` consecutive
+    columns (128: the layer's 1x128 format; 32: the MXFP8 1x32 format).
 
-    x: [R, C] fp64 (C % 128 == 0).  Returns (q, s): q [R, C] fp64 on the E4M3
-    grid (the stored FP8 values) and s [R, C/128] int64 exponents; the value
-    the GEMM consumes is q * 2^s.
+    x: [R, C] fp64 (C % group == 0).  Returns (q, s): q [R, C] fp64 on the
+    E4M3 grid (the stored FP8 values) and s [R, C/group] int64 exponents; the
+    value the GEMM consumes is q * 2^s.
     """
     x = np.asarray(x, dtype=np.float64)
     R, C = x.shape
-    if C % 128:
-        raise ValueError("quantisation groups are 128 columns wide")
-    g = x.reshape(R, C // 128, 128)
+    if C % group:
+        raise ValueError(f"quantisation groups are {group} columns wide")
+    g = x.reshape(R, C // group, group)
     s = ue8m0_exponent(np.abs(g).max(axis=2) if C else np.zeros((R, 0)))
     scaled = g * np.ldexp(1.0, -s)[..., None]   # exact: power-of-two factor
     q = e4m3_round(scaled)
     return q.reshape(R, C), s
 
 
+def dequant_groups(q, s, group):
+    """q [R, C] on the E4M3 grid and s [R, C/group] -> fp64 values q * 2^s."""
+    R, C = q.shape
+    return (q.reshape(R, C // group, group) * np.ldexp(1.0, s)[..., None]).reshape(R, C)
+
+
+def quant_fp8_1x128(x):
+    """The layer's activation format: ``quant_fp8_groups(x, 128)``."""
+    return quant_fp8_groups(x, 128)
+
+
 def dequant_1x128(q, s):
     """q [R, C] on the E4M3 grid and s [R, C/128] -> fp64 values q * 2^s."""
-    R, C = q.shape
-    return (q.reshape(R, C // 128, 128) * np.ldexp(1.0, s)[..., None]).reshape(R, C)
+    return dequant_groups(q, s, 128)
+
+
+def quant_mxfp8_1x32(x):
+    """MXFP8 activation format: E4M3 elements sharing one UE8M0 scale per 32
+    consecutive columns, the block size of the OCP microscaling formats.  The
+    exponent follows the layer's rule (smallest s with amax <= 448 * 2^s),
+    applied per 32-column block: ``quant_fp8_groups(x, 32)``."""
+    return quant_fp8_groups(x, 32)
 
 
 def exp2i(s):

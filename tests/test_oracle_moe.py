@@ -1,7 +1,7 @@
 """Pins for oracle.moe against things other than itself:
 
 * the layout path equals a per-token loop sum_j w_j * expert_{e_j}(x) with no
-  layout at all (bitwise), for FP8 and BF16, compact and masked;
+  layout at all (bitwise), for FP8, MXFP8 and BF16, compact and masked;
 * masked and compact layouts agree end to end (bitwise) -- the property the
   "Support DeepGEMM for standard MoE dispatch" report's end-to-end test checks;
 * k = 1 through a single expert is a textbook SwiGLU MLP, checked against
@@ -31,6 +31,11 @@ def small_problem(dtype, T=40, K=256, I=256, E_global=6, E_local=4, expert_start
         w2b, w2s = synth.fp8_expert_weights(E_local, K, I, seed + 1)
         w13 = oracle.dequant_fp8_weights(w13b.numpy(), w13s.numpy().astype(np.int64) - 127)
         w2 = oracle.dequant_fp8_weights(w2b.numpy(), w2s.numpy().astype(np.int64) - 127)
+    elif dtype == "mxfp8":
+        w13b, w13s = synth.mxfp8_expert_weights(E_local, 2 * I, K, seed)
+        w2b, w2s = synth.mxfp8_expert_weights(E_local, K, I, seed + 1)
+        w13 = oracle.dequant_mx_weights(w13b.numpy(), w13s.numpy().astype(np.int64) - 127)
+        w2 = oracle.dequant_mx_weights(w2b.numpy(), w2s.numpy().astype(np.int64) - 127)
     else:
         w13 = synth.bf16_expert_weights(E_local, 2 * I, K, seed).float().numpy().astype(np.float64)
         w2 = synth.bf16_expert_weights(E_local, K, I, seed + 1).float().numpy().astype(np.float64)
@@ -38,7 +43,7 @@ def small_problem(dtype, T=40, K=256, I=256, E_global=6, E_local=4, expert_start
                 expert_start=expert_start)
 
 
-@pytest.mark.parametrize("dtype", ["fp8", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
 def test_layout_path_equals_per_token_loop(dtype):
     p = small_problem(dtype)
     ref = oracle.forward_per_token(p["x"], p["w13"], p["w2"], p["topk_ids"], p["topk_weights"], dtype,
@@ -60,7 +65,7 @@ def test_dropped_tokens_give_zero_rows():
     assert np.all(out[none_local] == 0.0) and np.all(np.any(out[~none_local] != 0, axis=1))
 
 
-@pytest.mark.parametrize("dtype", ["fp8", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
 def test_single_expert_k1_is_textbook_swiglu(dtype):
     rng = np.random.default_rng(2)
     T, K, I = 16, 256, 384
