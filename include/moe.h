@@ -58,7 +58,9 @@ typedef enum {
 /* Arithmetic of the expert GEMMs [P1 "实现拆解" 1 and 3; P2 "实现拆解" 2]. */
 typedef enum {
   MOE_DTYPE_FP8_E4M3_UE8M0 = 0, /* FP8 e4m3 operands, UE8M0 scales: 1x128 (activations), 128x128 (weights) */
-  MOE_DTYPE_BF16 = 1            /* bf16 operands, no scales */
+  MOE_DTYPE_BF16 = 1,           /* bf16 operands, no scales */
+  MOE_DTYPE_MXFP8 = 2           /* FP8 e4m3 operands, one UE8M0 scale per 1x32 block for activations, h
+                                   and every weight row (the MXFP8 variant [P1 "风险与影响" 5]) */
 } moe_dtype_t;
 
 /* Row layout of the expert inputs [P1 "实现拆解" 2, "关键源码片段" deep_gemm.py]. */
@@ -103,9 +105,10 @@ typedef struct {
   uint64_t chunk_hist;  /* int32[E_local * chunks] plan scratch */
   uint64_t chunk_rank;  /* int32[T * topk]         plan scratch */
   uint64_t a;           /* [rows, K]  fp8 bytes or bf16: expert inputs */
-  uint64_t a_sf;        /* fp8: scale chunks of a (see moe_sf_offset) */
+  uint64_t a_sf;        /* fp8 / mxfp8: scale chunks of a (see moe_sf_offset); MXFP8 stores the four
+                           32-column scales of a row and 128-column group in the word's four bytes */
   uint64_t h;           /* [rows, I]  fp8 bytes or bf16: silu(gate) * up */
-  uint64_t h_sf;        /* fp8: scale chunks of h */
+  uint64_t h_sf;        /* fp8 / mxfp8: scale chunks of h */
   uint64_t y;           /* [rows, K]  bf16: expert outputs */
   int64_t rows;         /* rows of a / h / y */
   int64_t all_tokens;   /* compact static bound (0 for masked) */
@@ -128,12 +131,15 @@ int32_t moe_choose_layout(int32_t E_global, int32_t E_local);
 /* Create a context for one layer shape and its weights (device pointers):
  *   FP8:  w13 uint8 [E_local, 2I, K] e4m3, w13_sf uint8 [E_local, 2I/128, K/128] UE8M0,
  *         w2  uint8 [E_local, K, I]  e4m3, w2_sf  uint8 [E_local, K/128, I/128]  UE8M0
+ *   MXFP8: w13, w2 as for FP8; w13_sf / w2_sf hold one UE8M0 byte per row and
+ *         32-column block ([E_local, 2I, K/32] / [E_local, K, I/32]) in the
+ *         packed order moe_pack_mx_scales writes (16-byte aligned)
  *   BF16: w13 bf16 [E_local, 2I, K], w2 bf16 [E_local, K, I]; w13_sf = w2_sf = NULL
  * Rows 0..I-1 of w13[e] are the gate projection W1, rows I..2I-1 the up
  * projection W3 [P2 "关键源码片段" deep_gemm.py: the activation splits the
  * GEMM output in halves].  Weights are read, never written, and must stay
  * alive while the context is used.  A scale pointer given for BF16 or missing
- * for FP8 is MOE_ERR_DTYPE_MISMATCH.  Host-only: builds the weight TMA
+ * for FP8 / MXFP8 is MOE_ERR_DTYPE_MISMATCH.  Host-only: builds the weight TMA
  * descriptors; allocates no device memory. */
 moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uint8_t* w13_sf,
                             const void* w2, const uint8_t* w2_sf, moe_ctx** out);
@@ -247,6 +253,17 @@ moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_i
  * graph-capturable.  Inputs must be finite. */
 moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int64_t K, int32_t E_global,
                        int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
+
+/* Weight preparation for MOE_DTYPE_MXFP8, run once at load time: reorders
+ * the UE8M0 bytes of an MXFP8 weight tensor from the natural row-major
+ * layout src [E, N, C/32] (one byte per row and 32-column block, the OCP
+ * microscaling layout) into the packed order the grouped GEMMs copy into
+ * tensor memory: for every (e, 128-row block, 128-column group) a 512-byte
+ * chunk in which row r's four bytes (its four 32-column blocks, in column
+ * order) sit at 16 * (r % 32) + 4 * (r / 32).  dst has the same size as src
+ * and must not overlap it.  N and C must be multiples of 128; device
+ * pointers, 16-byte aligned; enqueued on stream. */
+moe_status_t moe_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C, void* stream);
 
 /* Number of kernel launches one moe_forward enqueues (for launch accounting). */
 int32_t moe_forward_launches(const moe_ctx* ctx);

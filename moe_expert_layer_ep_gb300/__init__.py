@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 MOE_DTYPE_FP8 = 0
 MOE_DTYPE_BF16 = 1
+MOE_DTYPE_MXFP8 = 2
 MOE_LAYOUT_AUTO = 0
 MOE_LAYOUT_COMPACT = 1
 MOE_LAYOUT_MASKED = 2
@@ -89,6 +90,7 @@ def _load():
         "moe_plan_layout_noalloc": (I32, [P(MoeShape), VP, P(MoePlanOutputs), VP]),
         "moe_requant_weights_ue8m0": (I32, [VP, VP, VP, VP, I64, I64, I64, VP]),
         "moe_route": (I32, [VP, VP, I64, I64, I32, I32, VP, VP, VP, VP]),
+        "moe_pack_mx_scales": (I32, [VP, VP, I64, I64, I64, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -103,7 +105,7 @@ EXPORTED = ("moe_compact_all_tokens", "moe_choose_layout", "moe_ctx_create", "mo
             "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2", "moe_combine", "moe_forward",
             "moe_forward_launches", "moe_read_device_status", "moe_clear_device_status",
             "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc",
-            "moe_requant_weights_ue8m0", "moe_route")
+            "moe_requant_weights_ue8m0", "moe_route", "moe_pack_mx_scales")
 
 
 def _check(code, what):
@@ -157,7 +159,12 @@ class MoeContext:
 
     @property
     def fp8(self):
-        return self.shape.dtype == MOE_DTYPE_FP8
+        """FP8 operands (1x128 / 128x128 or MXFP8 1x32 scales)."""
+        return self.shape.dtype in (MOE_DTYPE_FP8, MOE_DTYPE_MXFP8)
+
+    @property
+    def mx(self):
+        return self.shape.dtype == MOE_DTYPE_MXFP8
 
     @property
     def masked(self):
@@ -172,7 +179,7 @@ class MoeContext:
 def make_shape(T, K, I, E_global, E_local, topk, dtype, layout=MOE_LAYOUT_AUTO, expert_start=0, max_m=0,
                block_e=128):
     if isinstance(dtype, str):
-        dtype = {"fp8": MOE_DTYPE_FP8, "bf16": MOE_DTYPE_BF16}[dtype]
+        dtype = {"fp8": MOE_DTYPE_FP8, "bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8}[dtype]
     if isinstance(layout, str):
         layout = {"auto": MOE_LAYOUT_AUTO, "compact": MOE_LAYOUT_COMPACT, "masked": MOE_LAYOUT_MASKED}[layout]
     return MoeShape(T=T, K=K, I=I, E_global=E_global, E_local=E_local, expert_start=expert_start, topk=topk,
@@ -181,15 +188,16 @@ def make_shape(T, K, I, E_global, E_local, topk, dtype, layout=MOE_LAYOUT_AUTO, 
 
 def moe_ctx_create(shape, w13, w13_sf, w2, w2_sf):
     """shape: MoeShape; weights as in include/moe.h (CUDA tensors)."""
-    fp8 = shape.dtype == MOE_DTYPE_FP8
+    mx = shape.dtype == MOE_DTYPE_MXFP8
+    fp8 = shape.dtype == MOE_DTYPE_FP8 or mx
     E, K, I = shape.E_local, shape.K, shape.I
     wdt = torch.uint8 if fp8 else torch.bfloat16
     _require_cuda("w13", w13, wdt, E * 2 * I * K)
     _require_cuda("w2", w2, wdt, E * K * I)
     if w13_sf is not None:
-        _require_cuda("w13_sf", w13_sf, torch.uint8, E * (2 * I // 128) * (K // 128))
+        _require_cuda("w13_sf", w13_sf, torch.uint8, E * 2 * I * K // 32 if mx else E * (2 * I // 128) * (K // 128))
     if w2_sf is not None:
-        _require_cuda("w2_sf", w2_sf, torch.uint8, E * (K // 128) * (I // 128))
+        _require_cuda("w2_sf", w2_sf, torch.uint8, E * K * I // 32 if mx else E * (K // 128) * (I // 128))
     h = ctypes.c_void_p()
     _check(_lib.moe_ctx_create(ctypes.byref(shape), _ptr(w13), _ptr(w13_sf), _ptr(w2), _ptr(w2_sf),
                                ctypes.byref(h)), "moe_ctx_create")
@@ -308,6 +316,18 @@ def moe_route(x, w_router, topk, logits=None, topk_ids=None, topk_weights=None, 
     _check(_lib.moe_route(_ptr(x), _ptr(w_router), T, K, E, topk, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
                           _stream(stream)), "moe_route")
     return topk_ids, topk_weights, logits
+
+
+def moe_pack_mx_scales(sf, out=None, stream=None):
+    """MXFP8 weight scales uint8 [E, N, C/32] (natural layout) -> the packed
+    order moe_ctx_create takes for MOE_DTYPE_MXFP8 (see include/moe.h)."""
+    E, N, G = sf.shape
+    _require_cuda("sf", sf, torch.uint8)
+    if out is None:
+        out = torch.empty_like(sf)
+    _require_cuda("out", out, torch.uint8, sf.numel())
+    _check(_lib.moe_pack_mx_scales(_ptr(sf), _ptr(out), E, N, G * 32, _stream(stream)), "moe_pack_mx_scales")
+    return out
 
 
 def ws_view(ctx, ws, name):

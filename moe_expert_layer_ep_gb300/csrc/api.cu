@@ -15,7 +15,8 @@
 struct moe_ctx {
   moe_shape_t shape;
   int layout;  // resolved: MOE_LAYOUT_COMPACT or MOE_LAYOUT_MASKED
-  bool fp8;
+  bool fp8;   // FP8 operands (1x128 / 128x128 or MXFP8 scales)
+  bool mx;    // MXFP8: 1x32 scales
   const void* w13;
   const uint8_t* w13_sf;
   const void* w2;
@@ -78,7 +79,8 @@ moe_status_t check_shape(const moe_shape_t* s) {
       s->topk <= 0)
     return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s->E_local) + s->expert_start > s->E_global) return MOE_ERR_INVALID_ARG;
-  if (s->dtype != MOE_DTYPE_FP8_E4M3_UE8M0 && s->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_DTYPE_FP8_E4M3_UE8M0 && s->dtype != MOE_DTYPE_BF16 && s->dtype != MOE_DTYPE_MXFP8)
+    return MOE_ERR_INVALID_ARG;
   if (s->layout != MOE_LAYOUT_AUTO && s->layout != MOE_LAYOUT_COMPACT && s->layout != MOE_LAYOUT_MASKED)
     return MOE_ERR_INVALID_ARG;
   if (s->K % 128 || s->I % 128 || s->block_e != 128) return MOE_ERR_UNSUPPORTED;
@@ -169,6 +171,7 @@ moe::GemmArgs gemm_args(const moe_ctx* c, void* ws, int stage) {
   g.status = at<int32_t>(ws, c->ws.status);
   g.stage = stage;
   g.fp8 = c->fp8;
+  g.mx = c->mx;
   g.masked = c->layout == MOE_LAYOUT_MASKED;
   g.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
   const int64_t red = stage == 1 ? s.K : s.I;
@@ -220,10 +223,12 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   *out = nullptr;
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const bool fp8 = shape->dtype == MOE_DTYPE_FP8_E4M3_UE8M0;
+  const bool mx = shape->dtype == MOE_DTYPE_MXFP8;
+  const bool fp8 = shape->dtype == MOE_DTYPE_FP8_E4M3_UE8M0 || mx;
   if (!w13 || !w2) return MOE_ERR_INVALID_ARG;
   if (fp8 != (w13_sf != nullptr) || fp8 != (w2_sf != nullptr)) return MOE_ERR_DTYPE_MISMATCH;
   if (!aligned16(w13) || !aligned16(w2)) return MOE_ERR_MISALIGNED;
+  if (mx && (!aligned16(w13_sf) || !aligned16(w2_sf))) return MOE_ERR_MISALIGNED;
   int layout = shape->layout == MOE_LAYOUT_AUTO ? moe_choose_layout(shape->E_global, shape->E_local) : shape->layout;
   if (layout == MOE_LAYOUT_MASKED && shape->max_m < (shape->T > 0 ? shape->T : 1)) return MOE_ERR_INVALID_ARG;
   if (layout == MOE_LAYOUT_MASKED && static_cast<int64_t>(shape->E_local) * shape->max_m >= (int64_t(1) << 31))
@@ -236,6 +241,7 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   c->shape.layout = layout;
   c->layout = layout;
   c->fp8 = fp8;
+  c->mx = mx;
   c->w13 = w13;
   c->w13_sf = w13_sf;
   c->w2 = w2;
@@ -318,6 +324,7 @@ moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void*
   q.K = s.K;
   q.topk = s.topk;
   q.fp8 = ctx->fp8;
+  q.mx = ctx->mx;
   q.masked = ctx->layout == MOE_LAYOUT_MASKED;
   q.max_m = s.max_m;
   q.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
@@ -420,6 +427,17 @@ moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int
     return MOE_ERR_MISALIGNED;
   return cuda_status(moe::launch_route(x_bf16, w_router, T, K, E_global, topk, logits, topk_ids, topk_weights,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C, void* stream) {
+  if (E < 0 || N < 0 || C < 0) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || C % 128) return MOE_ERR_UNSUPPORTED;
+  if (E * N * C == 0) return MOE_OK;
+  if (!src || !dst) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_MISALIGNED;
+  const int64_t bytes = E * N * (C / 32);
+  if (src < dst + bytes && dst < src + bytes) return MOE_ERR_INVALID_ARG;   // overlap
+  return cuda_status(moe::launch_pack_mx_scales(src, dst, E, N, C, static_cast<cudaStream_t>(stream)));
 }
 
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {

@@ -14,6 +14,11 @@
 // are powers of two, they are handed to the block-scaled MMA
 // (kind::mxf8f6f4, one scale per 32 K-elements) by repeating each 1x128 scale
 // over its four 32-element sub-blocks: the products are the same, exactly.
+// The MXFP8 variant (1x32 scales everywhere; listed as uncovered in the
+// standard-dispatch report's "风险与影响" item 5) hands each 32-element
+// sub-block its own scale byte: the k-th MMA of a 128-byte K block reads byte
+// k of the scale words (scale-factor ID k), and the weight scales arrive as
+// packed chunks by bulk copy instead of being expanded in shared memory.
 //
 // Work unit: one 128-row expert block (from the block table written by the
 // plan) x one output column block.  Stage 1's B tile is 128 gate rows of w13
@@ -124,7 +129,7 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
 
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
-template <bool kFP8, int kStage>
+template <bool kFP8, bool kMX, int kStage>
 __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const GemmArgs g) {
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
       const int a_e = g.masked ? tl.expert : 0;
       uint32_t sg_cache = 0, su_cache = 0;
       for (int kb = 0; kb < k_blocks; ++kb) {
-        if (kFP8 && (kb & 31) == 0) {
+        if (kFP8 && !kMX && (kb & 31) == 0) {
           // weight scales of the next 32 K blocks, one per lane
           const int kk = kb + lane;
           if (kk < k_blocks) {
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
           ok = false;
           break;
         }
-        if (kFP8) {
+        if (kFP8 && !kMX) {
           // B scale tile: 256 rows, rows 0..127 share the first block's scale,
           // rows 128..255 the second's; 1 KB written by the warp.
           const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, kb & 31);
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
           __syncwarp();
         }
         if (lane == 0) {
-          const uint32_t bytes = kABytes + kBBytes + (kFP8 ? kSfaBytes : 0);
+          const uint32_t bytes = kABytes + kBBytes + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kc = kb * kElemsPerKBlock;
           tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
@@ -226,6 +231,17 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
           if (kFP8) {
             bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + sf_chunk_offset(tl.sf_block, kb, k_blocks),
                       kSfaBytes, &full[stage]);
+          }
+          if (kMX) {
+            // B scale tile: the packed 512-byte chunks of the two 128-row
+            // weight blocks (rows past the end of w2 are TMA zeros, so the
+            // clamped chunk's scales multiply zeros)
+            const int b0 = min(r0 >> 7, g.w_rows_blocks - 1);
+            const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
+            const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
+            uint8_t* sfb = smem + kOffSfb + stage * kSfbBytes;
+            bulk_load(sfb, g.w_sf + sf_chunk_offset(base + b0, kb, g.w_k_groups), 512, &full[stage]);
+            bulk_load(sfb + 512, g.w_sf + sf_chunk_offset(base + b1, kb, g.w_k_groups), 512, &full[stage]);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -285,8 +301,10 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
             tmem_cp_32x128b_x4(sfb_t + 4u, smem_desc(sfb_s + 512u, 16, 128, kSwizzleNone));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescFP8, sfa_t, sfb_t,
-                                   (kb | k) != 0);
+              mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
+                                   kMX ? (kIdescFP8 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4))
+                                       : kIdescFP8,
+                                   sfa_t, sfb_t, (kb | k) != 0);
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescBF16, (kb | k) != 0);
@@ -379,7 +397,39 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
           h[i] = silu_mul(__uint_as_float(g0[i]), __uint_as_float(u0[i]));
           h[32 + i] = silu_mul(__uint_as_float(g1[i]), __uint_as_float(u1[i]));
         }
-        if (kFP8) {
+        if (kMX) {
+          // MXFP8: this thread's 64 columns are two whole 32-column blocks,
+          // each with its own exponent; no exchange with the partner warp
+          if (row_ok) {
+            uint8_t* dstb = static_cast<uint8_t*>(g.out) + row * g.out_ld + tl.nb * 128 + 64 * half;
+            uint32_t sfw = 0;
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              float amax = 0.0f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[32 * blk + i]));
+              const int s = ue8m0_exponent(amax);
+              const float mul = exp2_neg(s);
+              uint4* dst = reinterpret_cast<uint4*>(dstb + 32 * blk);
+#pragma unroll
+              for (int v = 0; v < 2; ++v) {
+                const int b = 32 * blk + 16 * v;
+                uint4 o;
+                o.x = cvt_e4m3x2(h[b + 0] * mul, h[b + 1] * mul) | (cvt_e4m3x2(h[b + 2] * mul, h[b + 3] * mul) << 16);
+                o.y = cvt_e4m3x2(h[b + 4] * mul, h[b + 5] * mul) | (cvt_e4m3x2(h[b + 6] * mul, h[b + 7] * mul) << 16);
+                o.z = cvt_e4m3x2(h[b + 8] * mul, h[b + 9] * mul) |
+                      (cvt_e4m3x2(h[b + 10] * mul, h[b + 11] * mul) << 16);
+                o.w = cvt_e4m3x2(h[b + 12] * mul, h[b + 13] * mul) |
+                      (cvt_e4m3x2(h[b + 14] * mul, h[b + 15] * mul) << 16);
+                dst[v] = o;
+              }
+              sfw |= static_cast<uint32_t>(s + 127) << (8 * blk);
+            }
+            // bytes 2 * half and 2 * half + 1 of the row's scale word
+            *reinterpret_cast<uint16_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
+                                         sf_row_offset(r) + 2 * half) = static_cast<uint16_t>(sfw);
+          }
+        } else if (kFP8) {
           // 1x128 group = this thread's 64 columns + the partner warp's 64
           float amax = 0.0f;
 #pragma unroll
@@ -461,16 +511,16 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
   }
 }
 
-template <bool kFP8, int kStage>
+template <bool kFP8, bool kMX, int kStage>
 cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kStage>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kStage><<<grid, threads_for(kFP8, kStage), kSmemBytes, s>>>(a, b, g);
+  grouped_gemm_kernel<kFP8, kMX, kStage><<<grid, threads_for(kFP8, kStage), kSmemBytes, s>>>(a, b, g);
   return cudaGetLastError();
 }
 
@@ -494,10 +544,15 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 int gemm_smem_bytes(int) { return kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
-  if (g.fp8) {
-    return g.stage == 1 ? launch_one<true, 1>(g, a, b, grid, s) : launch_one<true, 2>(g, a, b, grid, s);
+  if (g.mx) {
+    return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, grid, s) : launch_one<true, true, 2>(g, a, b, grid, s);
   }
-  return g.stage == 1 ? launch_one<false, 1>(g, a, b, grid, s) : launch_one<false, 2>(g, a, b, grid, s);
+  if (g.fp8) {
+    return g.stage == 1 ? launch_one<true, false, 1>(g, a, b, grid, s)
+                        : launch_one<true, false, 2>(g, a, b, grid, s);
+  }
+  return g.stage == 1 ? launch_one<false, false, 1>(g, a, b, grid, s)
+                      : launch_one<false, false, 2>(g, a, b, grid, s);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {

@@ -42,6 +42,7 @@ struct QuantArgs {
   int64_t T, K;
   int32_t topk;
   int32_t fp8;
+  int32_t mx;               // fp8 with 1x32 scales (MXFP8)
   int32_t masked;
   int64_t max_m;
   int32_t blocks_per_expert;
@@ -65,6 +66,7 @@ struct GemmArgs {
   int32_t* status;
   int32_t stage;              // 1: w13 + SiLU*up, 2: w2
   int32_t fp8;
+  int32_t mx;                 // fp8 with 1x32 scales; w_sf in the packed chunk order
   int32_t masked;
   int32_t blocks_per_expert;  // masked
   int32_t n_blocks;           // output column blocks (128 h columns, or 256 y columns)
@@ -74,7 +76,7 @@ struct GemmArgs {
   int32_t w_rows_blocks;      // weight rows / 128 (for the weight-scale table)
   int32_t w_k_groups;         // reduction / 128 (weight-scale table)
   const uint8_t* a_sf;        // fp8: activation scale chunks
-  const uint8_t* w_sf;        // fp8: weight scales [E, rows/128, red/128]
+  const uint8_t* w_sf;        // fp8: weight scales [E, rows/128, red/128]; mxfp8: packed 512-byte chunks
   void* out;                  // h (stage 1) or y (stage 2)
   int64_t out_ld;             // output row stride in elements
   uint8_t* out_sf;            // stage 1 fp8: h scale chunks
@@ -89,6 +91,8 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUten
                         cudaStream_t s);
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t s);
+cudaError_t launch_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+                                  cudaStream_t s);
 cudaError_t launch_route(const void* x, const float* w, int64_t T, int64_t K, int E, int topk, float* logits,
                          int32_t* ids, float* wts, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);

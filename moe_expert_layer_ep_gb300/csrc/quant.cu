@@ -1,11 +1,14 @@
-// moe_quant_scatter: token rows -> expert rows, FP8 1x128 UE8M0 or BF16.
+// moe_quant_scatter: token rows -> expert rows, FP8 1x128 UE8M0, MXFP8 1x32
+// UE8M0, or BF16.
 //
 // "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
 // "实现拆解" step 3: activations are quantised directly with a power-of-two
 // (UE8M0) scale rather than quantised with a real scale whose value is
 // rounded afterwards.  For each 128-column group the exponent is the smallest
 // s with amax <= 448 * 2^s; every element is multiplied by 2^-s (exact) and
-// rounded to e4m3 (nearest even, saturating).  "Add BF16 support to EP-MoE for
+// rounded to e4m3 (nearest even, saturating).  MXFP8 applies the same rule
+// per 32-column block (the variant listed as uncovered in "风险与影响" item 5).
+// "Add BF16 support to EP-MoE for
 // DeepGEMM" (sglang PR #17392 report), "实现拆解" step 3: the BF16 path moves
 // the rows without scales.
 //
@@ -35,7 +38,9 @@ __device__ __forceinline__ void dest_block(const QuantArgs& q, int64_t d, int64_
   }
 }
 
-template <bool kFP8>
+// kMX: MXFP8, one exponent per 32 columns (4 lanes); the four exponents of a
+// 128-column group fill the four bytes of the row's scale word.
+template <bool kFP8, bool kMX>
 __global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs q) {
   __shared__ int64_t s_dst[kMaxTopk];
   __shared__ int64_t s_blk[kMaxTopk];
@@ -72,16 +77,23 @@ __global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs 
       float amax = 0.0f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      // 16 lanes = one 128-column group
+      // 16 lanes = one 128-column group (MXFP8: 4 lanes = one 32-column block)
 #pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      for (int o = kMX ? 2 : 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
       const int s = ue8m0_exponent(amax);
+      uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
+      if constexpr (kMX) {
+        const int lane = tid & 31;
+        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 4);
+        const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 8);
+        const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 12);
+        sf_word = static_cast<uint32_t>(s + 127) | (b1 << 8) | (b2 << 16) | (b3 << 24);   // valid at group leads
+      }
       const float mul = exp2_neg(s);
       uint2 packed;
       packed.x = cvt_e4m3x2(f[0] * mul, f[1] * mul) | (cvt_e4m3x2(f[2] * mul, f[3] * mul) << 16);
       packed.y = cvt_e4m3x2(f[4] * mul, f[5] * mul) | (cvt_e4m3x2(f[6] * mul, f[7] * mul) << 16);
       if (active) {
-        const uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
         const int64_t group = col >> 7;
         const bool group_lead = (tid & 15) == 0;
         for (int j = 0; j < q.topk; ++j) {
@@ -166,10 +178,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs c)
 
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s) {
   if (q.T <= 0) return cudaSuccess;
-  if (q.fp8)
-    quant_scatter_kernel<true><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
+  if (q.mx)
+    quant_scatter_kernel<true, true><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
+  else if (q.fp8)
+    quant_scatter_kernel<true, false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
   else
-    quant_scatter_kernel<false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
+    quant_scatter_kernel<false, false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
   return cudaGetLastError();
 }
 

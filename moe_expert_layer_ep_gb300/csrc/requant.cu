@@ -1,5 +1,8 @@
-// moe_requant_weights_ue8m0: load-time requantisation of 128x128
-// block-scaled FP8 weights to power-of-two (UE8M0) block scales.
+// Load-time weight preparation:
+//   moe_requant_weights_ue8m0: requantisation of 128x128 block-scaled FP8
+//     weights to power-of-two (UE8M0) block scales;
+//   moe_pack_mx_scales: MXFP8 weight scales into the chunk order the grouped
+//     GEMMs copy into tensor memory.
 //
 // "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
 // "实现拆解" step 1 and "关键源码片段" fp8.py: both expert weight tensors of
@@ -81,7 +84,32 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   if (tid == 0) s_out[blk] = static_cast<uint8_t>(s + 127);
 }
 
+// MXFP8 weight scales, natural [E, N, C/32] bytes -> packed 512-byte chunks
+// per (e, 128-row block, 128-column group), row r's word at byte
+// 16 * (r % 32) + 4 * (r / 32).  A source word (4 consecutive 32-column
+// blocks of one row) is a destination word, so one thread moves one word.
+__global__ void __launch_bounds__(256) pack_mx_scales_kernel(const uint32_t* src, uint32_t* dst, int64_t words,
+                                                             int64_t N, int64_t CG) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= words) return;
+  const int64_t kg = i % CG;          // 128-column group
+  const int64_t n = (i / CG) % N;     // row
+  const int64_t e = i / (CG * N);
+  const int r = static_cast<int>(n & 127);
+  const int64_t chunk = (e * (N / 128) + (n >> 7)) * CG + kg;
+  dst[chunk * 128 + 4 * (r & 31) + (r >> 5)] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+                                  cudaStream_t st) {
+  const int64_t words = E * N * (C / 128);
+  if (words <= 0) return cudaSuccess;
+  pack_mx_scales_kernel<<<static_cast<unsigned>((words + 255) / 256), 256, 0, st>>>(
+      reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(dst), words, N, C / 128);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t st) {

@@ -157,4 +157,9 @@ WORKLOADS = {
                             dtype="fp8", layout="compact", zipf_s=None, seed=0x4D6F45_0004),
     "fp8_masked_decode": dict(T=64, K=7168, I=2048, E_global=256, E_local=32, expert_start=0, topk=8,
                               dtype="fp8", layout="masked", zipf_s=None, seed=0x4D6F45_0003),
+    # the MXFP8 variant (1x32 UE8M0 scales everywhere) of the two shapes above
+    "mxfp8_prefill_zipf": dict(T=8192, K=7168, I=2048, E_global=256, E_local=256, expert_start=0, topk=8,
+                               dtype="mxfp8", layout="compact", zipf_s=1.2, seed=0x4D6F45_0003),
+    "mxfp8_masked_decode": dict(T=64, K=7168, I=2048, E_global=256, E_local=32, expert_start=0, topk=8,
+                                dtype="mxfp8", layout="masked", zipf_s=None, seed=0x4D6F45_0003),
 }

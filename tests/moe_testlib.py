@@ -43,6 +43,10 @@ class Problem:
         if dtype == "fp8":
             self.w13, self.w13_sf = synth.fp8_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
             self.w2, self.w2_sf = synth.fp8_expert_weights(E_local, K, I, ws + 1, weight_device, expert_start)
+        elif dtype == "mxfp8":
+            # natural [E, N, C/32] scale layout; GpuLayer packs it for the device
+            self.w13, self.w13_sf = synth.mxfp8_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
+            self.w2, self.w2_sf = synth.mxfp8_expert_weights(E_local, K, I, ws + 1, weight_device, expert_start)
         else:
             self.w13 = synth.bf16_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
             self.w2 = synth.bf16_expert_weights(E_local, K, I, ws + 1, weight_device, expert_start)
@@ -56,11 +60,10 @@ class Problem:
     def expert_weights64(self, e):
         """fp64 dequantised (w13[e], w2[e]) for local expert e (cached)."""
         if e not in self._deq:
-            if self.dtype == "fp8":
-                w13 = oracle.dequant_fp8_weights(self.w13[e:e + 1].cpu().numpy(),
-                                                 self.w13_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
-                w2 = oracle.dequant_fp8_weights(self.w2[e:e + 1].cpu().numpy(),
-                                                self.w2_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
+            if self.dtype in ("fp8", "mxfp8"):
+                deq = oracle.dequant_fp8_weights if self.dtype == "fp8" else oracle.dequant_mx_weights
+                w13 = deq(self.w13[e:e + 1].cpu().numpy(), self.w13_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
+                w2 = deq(self.w2[e:e + 1].cpu().numpy(), self.w2_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
             else:
                 w13 = bf16_to_f64(self.w13[e])
                 w2 = bf16_to_f64(self.w2[e])
@@ -119,6 +122,9 @@ class GpuLayer:
         self.w2 = p.w2.to(dev)
         self.w13_sf = None if p.w13_sf is None else p.w13_sf.to(dev)
         self.w2_sf = None if p.w2_sf is None else p.w2_sf.to(dev)
+        if p.dtype == "mxfp8":
+            self.w13_sf = M.moe_pack_mx_scales(self.w13_sf)
+            self.w2_sf = M.moe_pack_mx_scales(self.w2_sf)
         self.ctx = M.moe_ctx_create(self.shape, self.w13, self.w13_sf, self.w2, self.w2_sf)
         self.ws = M.alloc_workspace(self.ctx)
         self.x = p.x.to(dev)
@@ -155,7 +161,8 @@ class GpuLayer:
     # decoded views
     def sf_bytes(self, name, rows):
         """UE8M0 bytes of the given rows, [len(rows), groups] (row indices in
-        the a/h/y row space)."""
+        the a/h/y row space); MXFP8: [len(rows), 4 * groups], one byte per
+        32-column block."""
         L, s = self.ctx.ws_layout, self.p
         groups = (s.K if name == "a_sf" else s.I) // 128
         sf = self.view(name).cpu().numpy()
@@ -168,6 +175,8 @@ class GpuLayer:
             blk, r = rows // 128, rows % 128
         g = np.arange(groups)
         off = (blk[:, None] * groups + g[None, :]) * 512 + (16 * (r % 32) + 4 * (r // 32))[:, None]
+        if self.ctx.mx:
+            return sf[(off[:, :, None] + np.arange(4)[None, None, :]).reshape(len(rows), 4 * groups)]
         return sf[off]
 
     def decoded(self, name, rows):
@@ -179,4 +188,4 @@ class GpuLayer:
             return bf16_to_f64(sel)
         q = oracle.e4m3_from_bits(sel.numpy())
         s = self.sf_bytes(name + "_sf", rows).astype(np.int64) - 127
-        return oracle.dequant_1x128(q, s)
+        return oracle.dequant_groups(q, s, 32 if self.ctx.mx else 128)

@@ -2,7 +2,7 @@
 stage input (so a failure points at one kernel).
 
 Tolerances.  GEMM1: the oracle's fp64 h on the GPU's own dequantised a,
-stored the same way (FP8 1x128 UE8M0 or bf16): relative Frobenius error
+stored the same way (FP8 1x128 UE8M0, MXFP8 1x32 UE8M0 or bf16): relative Frobenius error
 <= 2e-3 (FP8 codes may differ by one step where the fp32 and fp64 values of h
 straddle a rounding boundary; the flip rate is bounded too).  GEMM2: the
 oracle's fp64 y on the GPU's own h, rounded to bf16: <= 2e-3.  Combine: the
@@ -26,6 +26,9 @@ CASES = [
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
     dict(T=600, K=512, I=256, E_global=32, E_local=32, topk=8, dtype="fp8", layout="compact", zipf_s=1.2),
+    dict(T=128, K=256, I=256, E_global=8, E_local=8, topk=2, dtype="mxfp8", layout="compact"),
+    dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="mxfp8", layout="compact", drop_every=5),
+    dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
 ]
 
 
@@ -64,7 +67,7 @@ def test_gemm1_act_matches_oracle(case):
         h_ref[sel], _ = oracle.store_act(h, p.dtype)
     err = rel_fro(h_gpu, h_ref)
     assert err <= 2e-3, err
-    if p.dtype == "fp8":
+    if p.dtype in ("fp8", "mxfp8"):
         flips = np.mean(h_gpu != h_ref)
         assert flips <= 5e-3, flips
 
