@@ -239,20 +239,35 @@ moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_i
  * MoE router GEMM is kept in fp32 so that expert selection does not flip under
  * deterministic inference; P1 "关键源码片段" deep_gemm.py: the layer takes
  * standard top-k ids and weights].
- *   logits[t, e] = sum_k x[t, k] * w_router[e, k] in fp32 (x bf16 [T, K], exact
- *     in fp32; w_router fp32 [E_global, K]); every logit sums its K products in
- *     four chains (k mod 4, ascending k) combined as (c0 + c1) + (c2 + c3),
- *     whatever T, so a token's results do not depend on its batch;
+ *
+ * moe_router_prepare (load time): splits the fp32 router weights w_router
+ * [E_global, K] into three bf16 planes w_planes [3, E_global, K] with
+ * plane0 + plane1 + plane2 == w exactly (for |w| >= 2^-110), so that the
+ * router's fp32 GEMM runs on the tensor cores with exact products.  K must be
+ * a multiple of 128; device pointers, 16-byte aligned; enqueued on stream.
+ *
+ * moe_route: for x bf16 [T, K] (device),
+ *   logits[t, e] = sum_k x[t, k] * w[e, k], products exact, accumulated in
+ *     fp32: per 1024-wide K segment on the tensor cores, then the segments
+ *     added in order.  The operations for one token do not depend on T, so a
+ *     token's results are the same bits at every batch size;
  *   topk_ids[t, :] int32 [T, topk]: the topk largest logits in descending
  *     order, equal logits ordered by the lower expert id;
  *   topk_weights[t, j] fp32 = exp(z_j - z_0) / sum_i exp(z_i - z_0) over the
  *     selected logits, the sum taken in j order.
- * K must be a multiple of 128, E_global <= 1024, topk <= min(64, E_global)
+ * ws: caller-owned device scratch of at least moe_route_workspace_size(T, K,
+ * E_global) bytes (MOE_ERR_BUFFER_TOO_SMALL otherwise); its first int32 is the
+ * device status word (cleared by each call; MOE_ERR_TIMEOUT if a bounded wait
+ * ran out), readable with moe_read_device_status(ws, ...).  K must be a
+ * multiple of 128, E_global <= 1024, topk <= min(64, E_global), T <= 2^30
  * (MOE_ERR_UNSUPPORTED otherwise); all pointers device, 16-byte aligned
- * (MOE_ERR_MISALIGNED); the caller owns every buffer; enqueued on stream,
- * graph-capturable.  Inputs must be finite. */
-moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int64_t K, int32_t E_global,
-                       int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* stream);
+ * (MOE_ERR_MISALIGNED); enqueued on stream, graph-capturable (the call
+ * encodes its TMA descriptors on the host).  Inputs must be finite. */
+int64_t moe_route_workspace_size(int64_t T, int64_t K, int32_t E_global);
+moe_status_t moe_router_prepare(const float* w_router, void* w_planes, int64_t E_global, int64_t K, void* stream);
+moe_status_t moe_route(const void* x_bf16, const void* w_planes, int64_t T, int64_t K, int32_t E_global,
+                       int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* ws,
+                       int64_t ws_bytes, void* stream);
 
 /* Weight preparation for MOE_DTYPE_MXFP8, run once at load time: reorders
  * the UE8M0 bytes of an MXFP8 weight tensor from the natural row-major

@@ -89,7 +89,9 @@ def _load():
         "moe_strerror": (ctypes.c_char_p, [I32]),
         "moe_plan_layout_noalloc": (I32, [P(MoeShape), VP, P(MoePlanOutputs), VP]),
         "moe_requant_weights_ue8m0": (I32, [VP, VP, VP, VP, I64, I64, I64, VP]),
-        "moe_route": (I32, [VP, VP, I64, I64, I32, I32, VP, VP, VP, VP]),
+        "moe_route": (I32, [VP, VP, I64, I64, I32, I32, VP, VP, VP, VP, I64, VP]),
+        "moe_route_workspace_size": (I64, [I64, I64, I32]),
+        "moe_router_prepare": (I32, [VP, VP, I64, I64, VP]),
         "moe_pack_mx_scales": (I32, [VP, VP, I64, I64, I64, VP]),
     }
     for name, (res, args) in sig.items():
@@ -105,7 +107,8 @@ EXPORTED = ("moe_compact_all_tokens", "moe_choose_layout", "moe_ctx_create", "mo
             "moe_grouped_gemm_w13_act", "moe_grouped_gemm_w2", "moe_combine", "moe_forward",
             "moe_forward_launches", "moe_read_device_status", "moe_clear_device_status",
             "moe_selftest_wait_timeout", "moe_sf_offset", "moe_strerror", "moe_plan_layout_noalloc",
-            "moe_requant_weights_ue8m0", "moe_route", "moe_pack_mx_scales")
+            "moe_requant_weights_ue8m0", "moe_route", "moe_pack_mx_scales", "moe_route_workspace_size",
+            "moe_router_prepare")
 
 
 def _check(code, what):
@@ -296,13 +299,30 @@ def moe_requant_weights_ue8m0(w_in, scale_in, w_out=None, scale_out=None, stream
     return w_out, scale_out
 
 
-def moe_route(x, w_router, topk, logits=None, topk_ids=None, topk_weights=None, stream=None):
-    """x bf16 [T, K], w_router fp32 [E, K] -> (topk_ids int32 [T, k],
-    topk_weights fp32 [T, k], logits fp32 [T, E]); see include/moe.h."""
+def moe_router_prepare(w_router, out=None, stream=None):
+    """fp32 router weights [E, K] -> bf16 planes [3, E, K] (hi + mid + lo == w);
+    see include/moe.h."""
+    E, K = w_router.shape
+    _require_cuda("w_router", w_router, torch.float32)
+    if out is None:
+        out = torch.empty((3, E, K), dtype=torch.bfloat16, device=w_router.device)
+    _require_cuda("out", out, torch.bfloat16, 3 * E * K)
+    _check(_lib.moe_router_prepare(_ptr(w_router), _ptr(out), E, K, _stream(stream)), "moe_router_prepare")
+    return out
+
+
+def moe_route_workspace_size(T, K, E):
+    return int(_lib.moe_route_workspace_size(T, K, E))
+
+
+def moe_route(x, w_planes, topk, logits=None, topk_ids=None, topk_weights=None, ws=None, stream=None):
+    """x bf16 [T, K], w_planes bf16 [3, E, K] (moe_router_prepare) ->
+    (topk_ids int32 [T, k], topk_weights fp32 [T, k], logits fp32 [T, E]);
+    see include/moe.h.  ws: uint8 device scratch (allocated here if None)."""
     T, K = x.shape
-    E = w_router.shape[0]
+    E = w_planes.shape[1]
     _require_cuda("x", x, torch.bfloat16)
-    _require_cuda("w_router", w_router, torch.float32, E * K)
+    _require_cuda("w_planes", w_planes, torch.bfloat16, 3 * E * K)
     dev = x.device
     if logits is None:
         logits = torch.empty((T, E), dtype=torch.float32, device=dev)
@@ -310,11 +330,14 @@ def moe_route(x, w_router, topk, logits=None, topk_ids=None, topk_weights=None, 
         topk_ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
     if topk_weights is None:
         topk_weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(16, moe_route_workspace_size(T, K, E)), dtype=torch.uint8, device=dev)
     _require_cuda("logits", logits, torch.float32, T * E)
     _require_cuda("topk_ids", topk_ids, torch.int32, T * topk)
     _require_cuda("topk_weights", topk_weights, torch.float32, T * topk)
-    _check(_lib.moe_route(_ptr(x), _ptr(w_router), T, K, E, topk, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
-                          _stream(stream)), "moe_route")
+    _require_cuda("ws", ws, torch.uint8)
+    _check(_lib.moe_route(_ptr(x), _ptr(w_planes), T, K, E, topk, _ptr(logits), _ptr(topk_ids), _ptr(topk_weights),
+                          _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
     return topk_ids, topk_weights, logits
 
 

@@ -415,17 +415,57 @@ moe_status_t moe_requant_weights_ue8m0(const uint8_t* w_in, const float* scale_i
   return cuda_status(moe::launch_requant(w_in, scale_in, w_out, scale_out, E, N, C, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_route(const void* x_bf16, const float* w_router, int64_t T, int64_t K, int32_t E_global,
-                       int32_t topk, float* logits, int32_t* topk_ids, float* topk_weights, void* stream) {
+int64_t moe_route_workspace_size(int64_t T, int64_t K, int32_t E_global) {
+  if (T < 0 || K <= 0 || E_global <= 0) return -1;
+  const int64_t segs = (K + moe::kRouterSegment - 1) / moe::kRouterSegment;
+  return 256 + static_cast<int64_t>(align_up(static_cast<uint64_t>(segs * T * E_global) * 4, 256));
+}
+
+moe_status_t moe_router_prepare(const float* w_router, void* w_planes, int64_t E_global, int64_t K, void* stream) {
+  if (E_global <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!w_router || !w_planes) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_router) || !aligned16(w_planes)) return MOE_ERR_MISALIGNED;
+  return cuda_status(moe::launch_router_split(w_router, static_cast<uint16_t*>(w_planes), E_global, K,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_route(const void* x_bf16, const void* w_planes, int64_t T, int64_t K, int32_t E_global, int32_t topk,
+                       float* logits, int32_t* topk_ids, float* topk_weights, void* ws, int64_t ws_bytes,
+                       void* stream) {
   if (T < 0 || K <= 0 || E_global <= 0 || topk <= 0) return MOE_ERR_INVALID_ARG;
-  if (K % 128 || E_global > moe::kMaxRouterExperts || topk > moe::kMaxTopk || topk > E_global)
+  if (K % 128 || E_global > moe::kMaxRouterExperts || topk > moe::kMaxTopk || topk > E_global ||
+      T > (int64_t(1) << 30))
     return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!x_bf16 || !w_router || !logits || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x_bf16) || !aligned16(w_router) || !aligned16(logits) || !aligned16(topk_ids) ||
-      !aligned16(topk_weights))
+  if (!x_bf16 || !w_planes || !logits || !topk_ids || !topk_weights || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_bf16) || !aligned16(w_planes) || !aligned16(logits) || !aligned16(topk_ids) ||
+      !aligned16(topk_weights) || !aligned16(ws))
     return MOE_ERR_MISALIGNED;
-  return cuda_status(moe::launch_route(x_bf16, w_router, T, K, E_global, topk, logits, topk_ids, topk_weights,
+  if (ws_bytes < moe_route_workspace_size(T, K, E_global)) return MOE_ERR_BUFFER_TOO_SMALL;
+  CUtensorMap map_x, map_w;
+  moe_status_t st = make_map(&map_x, x_bf16, false, static_cast<uint64_t>(K), static_cast<uint64_t>(T), 1);
+  if (st == MOE_OK)
+    st = make_map(&map_w, w_planes, false, static_cast<uint64_t>(K), static_cast<uint64_t>(E_global), 3);
+  if (st != MOE_OK) return st;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe::RouterArgs r;
+  memset(&r, 0, sizeof(r));
+  r.T = T;
+  r.K = K;
+  r.E = E_global;
+  r.segs = static_cast<int32_t>((K + moe::kRouterSegment - 1) / moe::kRouterSegment);
+  r.m_tiles = static_cast<int32_t>((T + 127) / 128);
+  r.n_tiles = (E_global + 127) / 128;
+  r.status = static_cast<int32_t*>(ws);
+  r.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  r.timeout_ns = 2000000000ull;
+  const int64_t items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * r.segs;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  return cuda_status(moe::launch_route(map_x, map_w, r, grid, topk, logits, topk_ids, topk_weights,
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -12,7 +12,7 @@ constexpr int kMaxLocalExperts = 1024;
 constexpr int kMaxTopk = 64;
 constexpr int kBlockM = 128;      // rows per expert block == compact block_e
 constexpr int kMaxRouterExperts = 1024;
-constexpr int kRouterSmallBatch = 256;   // router batches up to this size take the small-batch kernel
+constexpr int kRouterSegment = 1024;     // K elements per router partial sum (fixed, batch-independent)
 
 struct PlanArgs {
   const int32_t* topk_ids;  // [A]
@@ -93,8 +93,19 @@ cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_ou
                            int64_t N, int64_t C, cudaStream_t s);
 cudaError_t launch_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C,
                                   cudaStream_t s);
-cudaError_t launch_route(const void* x, const float* w, int64_t T, int64_t K, int E, int topk, float* logits,
-                         int32_t* ids, float* wts, cudaStream_t s);
+struct RouterArgs {
+  int64_t T, K;
+  int32_t E;
+  int32_t segs;             // ceil(K / kRouterSegment)
+  int32_t m_tiles, n_tiles; // ceil(T / 128), ceil(E / 128)
+  float* partial;           // [segs, T, E] fp32
+  int32_t* status;          // int32[4], cleared by the launch
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_router_split(const float* w, uint16_t* planes, int64_t E, int64_t K, cudaStream_t s);
+cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, const RouterArgs& r, int grid, int topk,
+                         float* logits, int32_t* ids, float* wts, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
 int plan_launches();

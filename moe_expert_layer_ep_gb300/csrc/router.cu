@@ -7,20 +7,22 @@
 // "Support DeepGEMM for standard MoE dispatch" (sglang PR #33128 report),
 // "关键源码片段" deep_gemm.py: the layer consumes standard top-k ids/weights.
 //
-//   router_logits_kernel        z[t, e] = sum_k x[t, k] * W[e, k], bf16 x (exact
-//                               in fp32) times fp32 W, fp32 FMA on the CUDA
-//                               cores; 64x64 output tiles, K in slabs of 32
-//                               through shared memory (large batches).
-//   router_logits_small_kernel  8 tokens x 2 experts per CTA with 1024-wide K
-//                               slabs, so that many CTAs stream the router
-//                               weights (batches of up to 256 tokens).
-//   Both sum every output's K terms in four fixed chains (k mod 4, ascending
-//   k), combined as (c0 + c1) + (c2 + c3): the same operations for every tile
-//   shape and batch size, so a token's logits do not depend on its batch.
-//   topk_softmax_kernel         one warp per token: k rounds of a warp argmax
-//                               (larger logit wins, equal logits go to the
-//                               lower expert id), then w_j = exp(z_j - z_max) /
-//                               sum, the sum taken in j order.
+// The fp32 GEMM runs on the tensor cores.  At load time every fp32 weight is
+// split into three bf16 planes with hi + mid + lo == w exactly
+// (router_split_kernel); x is bf16, so each product x * plane is exact in the
+// fp32 accumulator and z = x.hi + x.mid + x.lo is the fp32-accumulated fp32
+// product.
+//   router_logits_tc_kernel  persistent, TMA-fed tcgen05 kernel over work
+//                            items (128 tokens x 128 experts x one 1024-wide K
+//                            segment); 12 bf16 MMAs per 64-wide K block into a
+//                            TMEM accumulator; fp32 partials per segment.
+//   topk_softmax_kernel      one warp per token: folds the partials in
+//                            segment order into the logits, then k rounds of
+//                            a warp argmax (larger logit wins, equal logits go
+//                            to the lower expert id), then
+//                            w_j = exp(z_j - z_max) / sum, the sum in j order.
+// Tiles, segments and the fold order do not depend on the batch, so a
+// token's logits, ids and weights are the same bits at every batch size.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,186 +30,272 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouterThreads = 256;
+constexpr int kRtTileM = 128;                   // tokens per tile
+constexpr int kRtTileN = 128;                   // experts per tile
+constexpr int kRtKBlock = 64;                   // bf16 elements of K per stage (one 128-byte swizzle row)
+constexpr int kRtStages = 3;
+constexpr int kRtPlanes = 3;
+constexpr int kRtABytes = kRtTileM * 128;                  // 16 KB
+constexpr int kRtBPlaneBytes = kRtTileN * 128;             // 16 KB per plane
+constexpr int kRtBBytes = kRtPlanes * kRtBPlaneBytes;      // 48 KB
+constexpr int kRtOffA = 0;
+constexpr int kRtOffB = kRtOffA + kRtStages * kRtABytes;
+constexpr int kRtOffBar = kRtOffB + kRtStages * kRtBBytes;
+constexpr int kRtNumBars = 2 * kRtStages + 2 + 2 + 1;
+constexpr int kRtOffHolder = kRtOffBar + kRtNumBars * 8;
+constexpr int kRtOffAbort = kRtOffHolder + 8;
+constexpr int kRtSmemBytes = kRtOffAbort + 8 + 1024;      // + 1024-byte alignment slack
+constexpr uint32_t kRtTmemCols = 2 * kRtTileN;             // two accumulators
+constexpr int kRtThreads = 64 + 128;                       // producer, MMA, 4 epilogue warps
+constexpr uint32_t kRtIdesc = (1u << 4)                    // D f32
+                              | (1u << 7) | (1u << 10)     // A, B bf16
+                              | (static_cast<uint32_t>(kRtTileN >> 3) << 17) |
+                              (static_cast<uint32_t>(kRtTileM >> 4) << 24);
+static_assert(kRtSmemBytes <= 227 * 1024, "shared memory");
 
-// One BM x BN output tile per CTA (16 x 16 threads, each TM x TN outputs), K
-// in slabs of RK staged through shared memory (k-major) while the next slab
-// is already loaded into registers.
-template <int BM, int BN, int RK>
-__global__ void __launch_bounds__(kRouterThreads, 2) router_logits_kernel(const uint16_t* x, const float* w, float* z,
-                                                                       int64_t T, int64_t K, int E) {
-  constexpr int TM = BM / 16, TN = BN / 16;
-  constexpr int XV = BM * RK / 8 / kRouterThreads;   // 8-element bf16 vectors per thread per slab
-  constexpr int WV = BN * RK / 4 / kRouterThreads;   // 4-element fp32 vectors per thread per slab
-  static_assert(XV >= 1 && WV >= 1, "tile too small for the thread count");
-  __shared__ __align__(16) float xs[RK][BM];
-  __shared__ __align__(16) float ws[RK][BN];
-  const int tid = threadIdx.x;
-  const int ty = tid >> 4, tx = tid & 15;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BM;
-  const int e0 = blockIdx.y * BN;
-  float acc[4][TM][TN] = {};
-  uint4 xr[XV];
-  float4 wr[WV];
-  auto load = [&](int64_t k0) {
-#pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 8), kk = (i % (RK / 8)) * 8;
-      const int64_t t = t0 + r;
-      xr[v] = t < T ? __ldg(reinterpret_cast<const uint4*>(x + t * K + k0 + kk)) : make_uint4(0, 0, 0, 0);
+struct RtItem {
+  int mt, nt, seg, kb0, nkb;
+};
+
+__device__ __forceinline__ RtItem rt_item(const RouterArgs& r, int64_t i) {
+  RtItem it;
+  it.seg = static_cast<int>(i % r.segs);
+  it.nt = static_cast<int>((i / r.segs) % r.n_tiles);
+  it.mt = static_cast<int>(i / (static_cast<int64_t>(r.segs) * r.n_tiles));
+  it.kb0 = it.seg * (kRouterSegment / kRtKBlock);
+  const int kbs = static_cast<int>(r.K / kRtKBlock);
+  it.nkb = min(kRouterSegment / kRtKBlock, kbs - it.kb0);
+  return it;
+}
+
+// One work item: a 128-token x 128-expert tile of one K segment.  Per 64-wide
+// K block, 4 K-steps x 3 weight planes = 12 MMAs in the fixed order (step,
+// plane), all into one fp32 accumulator; the segment's partial logits go to
+// partial[seg][t][e].  A token's partials are the same operations whatever
+// the batch (tile rows are independent), so the folded logits are too.
+__global__ void __launch_bounds__(kRtThreads, 1)
+    router_logits_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                            const RouterArgs r) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRtOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kRtStages;
+  uint64_t* tfull = bars + 2 * kRtStages;
+  uint64_t* tempty = bars + 2 * kRtStages + 2;
+  uint64_t* done = bars + 2 * kRtStages + 4;
+  uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kRtOffHolder);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kRtOffAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-#pragma unroll
-    for (int v = 0; v < WV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 4), kk = (i % (RK / 4)) * 4;
-      const int e = e0 + r;
-      wr[v] = e < E ? __ldg(reinterpret_cast<const float4*>(w + static_cast<int64_t>(e) * K + k0 + kk))
-                    : make_float4(0, 0, 0, 0);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
     }
-  };
-  auto stage = [&]() {
-#pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 8), kk = (i % (RK / 8)) * 8;
-      const float2 p0 = unpack_bf16x2(xr[v].x), p1 = unpack_bf16x2(xr[v].y), p2 = unpack_bf16x2(xr[v].z),
-                   p3 = unpack_bf16x2(xr[v].w);
-      xs[kk + 0][r] = p0.x; xs[kk + 1][r] = p0.y; xs[kk + 2][r] = p1.x; xs[kk + 3][r] = p1.y;
-      xs[kk + 4][r] = p2.x; xs[kk + 5][r] = p2.y; xs[kk + 6][r] = p3.x; xs[kk + 7][r] = p3.y;
-    }
-#pragma unroll
-    for (int v = 0; v < WV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 4), kk = (i % (RK / 4)) * 4;
-      ws[kk + 0][r] = wr[v].x; ws[kk + 1][r] = wr[v].y; ws[kk + 2][r] = wr[v].z; ws[kk + 3][r] = wr[v].w;
-    }
-  };
-  load(0);
-  for (int64_t k0 = 0; k0 < K; k0 += RK) {   // K is a multiple of 128, so of RK
-    stage();
-    __syncthreads();
-    if (k0 + RK < K) load(k0 + RK);
-#pragma unroll
-    for (int k = 0; k < RK; ++k) {
-      float a[TM], b[TN];
-#pragma unroll
-      for (int i = 0; i < TM; ++i) a[i] = xs[k][ty * TM + i];
-#pragma unroll
-      for (int j = 0; j < TN; ++j) b[j] = ws[k][tx * TN + j];
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[k & 3][i][j] = fmaf(a[i], b[j], acc[k & 3][i][j]);
-    }
-    __syncthreads();
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&map_x);
+    prefetch_tensormap(&map_w);
   }
-#pragma unroll
-  for (int i = 0; i < TM; ++i) {
-    const int64_t t = t0 + ty * TM + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < TN; ++j) {
-      const int e = e0 + tx * TN + j;
-      if (e < E) z[t * E + e] = (acc[0][i][j] + acc[1][i][j]) + (acc[2][i][j] + acc[3][i][j]);
+  if (warp == 1) {
+    tmem_alloc(holder, kRtTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *holder;
+  const int64_t n_items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * r.segs;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const RtItem it = rt_item(r, i);
+        for (int kb = 0; kb < it.nkb; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, r.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kRtABytes + kRtBBytes);
+          const int kc = (it.kb0 + kb) * kRtKBlock;
+          tma_load_3d(smem + kRtOffA + stage * kRtABytes, &map_x, &full[stage], kc, it.mt * kRtTileM, 0);
+          for (int p = 0; p < kRtPlanes; ++p)
+            tma_load_3d(smem + kRtOffB + stage * kRtBBytes + p * kRtBPlaneBytes, &map_w, &full[stage], kc,
+                        it.nt * kRtTileN, p);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kRtStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(r.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // never leave the CTA with bulk copies still landing in its shared memory
+      const int never = 0;
+      for (int s = 0; s < kRtStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait_bounded(&full[s], (issued_parity >> s) & 1u, &never, r.timeout_ns);
     }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int iter = 0;
+      bool ok = true;
+      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++iter) {
+        const RtItem it = rt_item(r, i);
+        const int acc = iter & 1;
+        if (!mbar_wait_bounded(&tempty[acc], ((iter >> 1) & 1) ^ 1, abort_flag, r.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kRtTileN);
+        for (int kb = 0; kb < it.nkb; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, r.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = smem_desc(smem_u32(smem + kRtOffA + stage * kRtABytes), 16, 1024, kSwizzle128B);
+          const uint32_t b_addr = smem_u32(smem + kRtOffB + stage * kRtBBytes);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int p = 0; p < kRtPlanes; ++p)
+              mma_bf16(d_tmem, a_desc + 2 * k,
+                       smem_desc(b_addr + p * kRtBPlaneBytes, 16, 1024, kSwizzle128B) + 2 * k, kRtIdesc,
+                       (kb | k | p) != 0);
+          tc_commit(&empty[stage]);
+          if (++stage == kRtStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+      }
+      if (!ok) {
+        set_status(r.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      tc_commit(done);
+      const int never = 0;
+      mbar_wait_bounded(done, 0, &never, r.timeout_ns);
+    }
+  } else {
+    const int quad = warp & 3;   // tensor-memory lane quadrant this warp may read
+    int iter = 0;
+    for (int64_t i = blockIdx.x; i < n_items; i += gridDim.x, ++iter) {
+      const RtItem it = rt_item(r, i);
+      const int acc = iter & 1;
+      const bool got = mbar_wait_bounded(&tfull[acc], (iter >> 1) & 1, abort_flag, r.timeout_ns);
+      if (!__all_sync(0xFFFFFFFFu, got)) {
+        set_status(r.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int64_t t = static_cast<int64_t>(it.mt) * kRtTileM + quad * 32 + lane;
+      const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kRtTileN) + (static_cast<uint32_t>(quad * 32) << 16);
+      float* dst = r.partial + (static_cast<int64_t>(it.seg) * r.T + t) * r.E;
+#pragma unroll 1
+      for (int c = 0; c < kRtTileN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, v);
+        tmem_ld_wait();
+        if (c == kRtTileN / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
+        const int e0 = it.nt * kRtTileN + c * 32;
+        if (t < r.T && e0 < r.E) {
+          if (e0 + 32 <= r.E && (r.E & 3) == 0) {
+            float4* d4 = reinterpret_cast<float4*>(dst + e0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (e0 + j < r.E) dst[e0 + j] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kRtTmemCols);
   }
 }
 
-// Small batches: BM tokens x BN experts per CTA, one thread per output, the
-// whole CTA loading wide K slabs.  Shared rows are padded by four floats so
-// that the rows fall in distinct banks.
-template <int BM, int BN, int RK>
-__global__ void __launch_bounds__(kRouterThreads) router_logits_small_kernel(const uint16_t* x, const float* w,
-                                                                             float* z, int64_t T, int64_t K, int E) {
-  constexpr int XV = BM * RK / 8 / kRouterThreads;
-  constexpr int WV = BN * RK / 4 / kRouterThreads;
-  constexpr int LD = RK + 4;
-  static_assert(XV >= 1 && WV >= 1 && BM * BN <= kRouterThreads, "tile");
-  __shared__ __align__(16) float xs[BM][LD];
-  __shared__ __align__(16) float ws[BN][LD];
-  const int tid = threadIdx.x;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * BM;
-  const int e0 = blockIdx.y * BN;
-  const int my_r = tid / BN, my_c = tid % BN;
-  float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
-  uint4 xr[XV];
-  float4 wr[WV];
-  auto load = [&](int64_t k0) {
+// Load-time split of fp32 router weights into three bf16 planes with
+// hi + mid + lo == w exactly (each residual is exact in fp32 and the last
+// one has at most 8 significant bits) for |w| >= 2^-110.
+__global__ void __launch_bounds__(256) router_split_kernel(const float4* w, uint2* hi, uint2* mid, uint2* lo,
+                                                           int64_t n4) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = w[i];
+  const float in[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[4], m[4], l[4];
 #pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 8), kk = (i % (RK / 8)) * 8;
-      const int64_t t = t0 + r;
-      xr[v] = (t < T && k0 + kk < K) ? __ldg(reinterpret_cast<const uint4*>(x + t * K + k0 + kk))
-                                     : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int v = 0; v < WV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 4), kk = (i % (RK / 4)) * 4;
-      const int e = e0 + r;
-      wr[v] = (e < E && k0 + kk < K)
-                  ? __ldg(reinterpret_cast<const float4*>(w + static_cast<int64_t>(e) * K + k0 + kk))
-                  : make_float4(0, 0, 0, 0);
-    }
-  };
-  load(0);
-  for (int64_t k0 = 0; k0 < K; k0 += RK) {
-#pragma unroll
-    for (int v = 0; v < XV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 8), kk = (i % (RK / 8)) * 8;
-      const float2 p0 = unpack_bf16x2(xr[v].x), p1 = unpack_bf16x2(xr[v].y), p2 = unpack_bf16x2(xr[v].z),
-                   p3 = unpack_bf16x2(xr[v].w);
-      *reinterpret_cast<float4*>(&xs[r][kk]) = make_float4(p0.x, p0.y, p1.x, p1.y);
-      *reinterpret_cast<float4*>(&xs[r][kk + 4]) = make_float4(p2.x, p2.y, p3.x, p3.y);
-    }
-#pragma unroll
-    for (int v = 0; v < WV; ++v) {
-      const int i = tid + v * kRouterThreads;
-      const int r = i / (RK / 4), kk = (i % (RK / 4)) * 4;
-      *reinterpret_cast<float4*>(&ws[r][kk]) = wr[v];
-    }
-    __syncthreads();
-    if (k0 + RK < K) load(k0 + RK);
-    if (tid < BM * BN) {
-      // K is a multiple of 128, so a slab holds whole groups of four; the
-      // last slab stops at K (an extra zero product could flip a -0 sum).
-      const int kn = static_cast<int>(K - k0 < RK ? K - k0 : RK);
-#pragma unroll 4
-      for (int k = 0; k < kn; k += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(&xs[my_r][k]);
-        const float4 b = *reinterpret_cast<const float4*>(&ws[my_c][k]);
-        c0 = fmaf(a.x, b.x, c0);
-        c1 = fmaf(a.y, b.y, c1);
-        c2 = fmaf(a.z, b.z, c2);
-        c3 = fmaf(a.w, b.w, c3);
-      }
-    }
-    __syncthreads();
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat16 b1 = __float2bfloat16_rn(in[j]);
+    const float r1 = in[j] - __bfloat162float(b1);
+    const __nv_bfloat16 b2 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(b2);
+    const __nv_bfloat16 b3 = __float2bfloat16_rn(r2);
+    h[j] = __bfloat16_as_ushort(b1);
+    m[j] = __bfloat16_as_ushort(b2);
+    l[j] = __bfloat16_as_ushort(b3);
   }
-  const int64_t t = t0 + my_r;
-  const int e = e0 + my_c;
-  if (tid < BM * BN && t < T && e < E) z[t * E + e] = (c0 + c1) + (c2 + c3);
+  hi[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+  mid[i] = make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
+  lo[i] = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
 }
 
 // P logits per lane (E <= 32 P).  The j-th selection is kept by lane j % 32
 // (slot j / 32), so nothing is indexed dynamically; every lane forms the same
 // softmax sum in j order from broadcasts, and lane j writes output j.
 template <int P>
-__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* z, int64_t T, int E, int topk, int32_t* ids,
-                                                           float* wts) {
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* partial, int segs, int64_t T, int E,
+                                                           int topk, float* z, int32_t* ids, float* wts) {
   static_assert(P <= 32, "taken mask is 32 bits");
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   float v[P];
-  const float* row = z + t * E;
+  // logits = the segments' partial sums folded in segment order
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? row[e] : -INFINITY;
+    if (e < E) {
+      float acc = partial[t * E + e];
+      for (int sg = 1; sg < segs; ++sg) acc += partial[(static_cast<int64_t>(sg) * T + t) * E + e];
+      v[i] = acc;
+      z[t * E + e] = acc;
+    } else {
+      v[i] = -INFINITY;
+    }
   }
   uint32_t taken = 0;      // bit i: element lane + 32 i already selected
   float my_v0 = 0.0f, my_v1 = 0.0f;
@@ -258,27 +346,39 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* z, int64
 
 }  // namespace
 
-cudaError_t launch_route(const void* x, const float* w, int64_t T, int64_t K, int E, int topk, float* logits,
-                         int32_t* ids, float* wts, cudaStream_t s) {
-  if (T <= 0) return cudaSuccess;
-  const uint16_t* xb = static_cast<const uint16_t*>(x);
-  if (T <= kRouterSmallBatch) {
-    dim3 grid(static_cast<unsigned>((T + 7) / 8), static_cast<unsigned>((E + 1) / 2));
-    router_logits_small_kernel<8, 2, 1024><<<grid, kRouterThreads, 0, s>>>(xb, w, logits, T, K, E);
-  } else {
-    dim3 grid(static_cast<unsigned>((T + 63) / 64), static_cast<unsigned>((E + 63) / 64));
-    router_logits_kernel<64, 64, 32><<<grid, kRouterThreads, 0, s>>>(xb, w, logits, T, K, E);
+cudaError_t launch_router_split(const float* w, uint16_t* planes, int64_t E, int64_t K, cudaStream_t s) {
+  const int64_t n = E * K;
+  if (n <= 0) return cudaSuccess;
+  const int64_t n4 = n / 4;   // K is a multiple of 128
+  router_split_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(w), reinterpret_cast<uint2*>(planes), reinterpret_cast<uint2*>(planes + n),
+      reinterpret_cast<uint2*>(planes + 2 * n), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, const RouterArgs& r, int grid, int topk,
+                         float* logits, int32_t* ids, float* wts, cudaStream_t s) {
+  if (r.T <= 0) return cudaSuccess;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kRtSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
+  cudaError_t e = cudaMemsetAsync(r.status, 0, 16, s);
+  if (e != cudaSuccess) return e;
+  router_logits_tc_kernel<<<grid, kRtThreads, kRtSmemBytes, s>>>(map_x, map_w, r);
   const int warps = 8;
-  const unsigned nb = static_cast<unsigned>((T + warps - 1) / warps);
-  if (E <= 128)
-    topk_softmax_kernel<4><<<nb, warps * 32, 0, s>>>(logits, T, E, topk, ids, wts);
-  else if (E <= 256)
-    topk_softmax_kernel<8><<<nb, warps * 32, 0, s>>>(logits, T, E, topk, ids, wts);
-  else if (E <= 512)
-    topk_softmax_kernel<16><<<nb, warps * 32, 0, s>>>(logits, T, E, topk, ids, wts);
+  const unsigned nb = static_cast<unsigned>((r.T + warps - 1) / warps);
+  if (r.E <= 128)
+    topk_softmax_kernel<4><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
+  else if (r.E <= 256)
+    topk_softmax_kernel<8><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
+  else if (r.E <= 512)
+    topk_softmax_kernel<16><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
   else
-    topk_softmax_kernel<32><<<nb, warps * 32, 0, s>>>(logits, T, E, topk, ids, wts);
+    topk_softmax_kernel<32><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
   return cudaGetLastError();
 }
 

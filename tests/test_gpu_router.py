@@ -1,6 +1,9 @@
 """CUDA fp32 router vs the oracle.
 
-Logits: against fp64 within the error bound of a K-term fp32 sum.  Top-k ids:
+Logits: against fp64 within 2^-24 * K * sum|x w| -- the bound of a K-term
+sequential fp32 sum, which also covers the tensor-core path (exact products,
+3K/16 + 16 fp32 accumulations of at most 2^-23 relative error each, then
+the segment fold).  Top-k ids:
 bit-exact against the oracle's selection applied to the kernel's own fp32
 logits (the comparison that decides an id is taken in the kernel's
 precision), including rows with tied logits.  Weights: the oracle's softmax
@@ -26,8 +29,12 @@ def _inputs(T, K, E, seed):
     return x, w
 
 
+def _planes(w):
+    return M.moe_router_prepare(w.cuda())
+
+
 def _check(x, w, topk, rows=None):
-    ids, wts, z = M.moe_route(x.cuda(), w.cuda(), topk)
+    ids, wts, z = M.moe_route(x.cuda(), _planes(w), topk)
     torch.cuda.synchronize()
     z = z.cpu().numpy()
     ids = ids.cpu().numpy()
@@ -72,17 +79,18 @@ def test_router_full_size_sampled_and_batch_invariant():
     ids, wts, z = _check(x, w, 8, rows=[0, 1, 4095, 8191])
     # the same tokens routed in a batch of 7 give the same bits
     sub = torch.cat([x[4095:4096], x[:3], x[8191:8192], x[1:4]])
-    ids2, wts2, z2 = M.moe_route(sub.cuda(), w.cuda(), 8)
+    ids2, wts2, z2 = M.moe_route(sub.cuda(), _planes(w), 8)
     torch.cuda.synchronize()
     assert np.array_equal(z2.cpu().numpy()[0], z[4095]) and np.array_equal(z2.cpu().numpy()[4], z[8191])
     assert np.array_equal(ids2.cpu().numpy()[1:4], ids[:3]) and np.array_equal(wts2.cpu().numpy()[4], wts[8191])
 
 
 def test_router_logits_identical_across_batch_sizes():
-    """Batches of 1, 40, 256 and 300 tokens take different kernels and
-    tilings; every token's logits, ids and weights are the same bits."""
+    """Batches of 1, 40, 256 and 300 tokens cover one to three token tiles
+    and a ragged K segment; every token's logits, ids and weights are the
+    same bits."""
     x, w = _inputs(300, 1152, 37, 5)
-    wc = w.cuda()
+    wc = _planes(w)
     full = [t.cpu() for t in M.moe_route(x.cuda(), wc, 6)]
     for n in (1, 40, 256):
         part = [t.cpu() for t in M.moe_route(x[:n].cuda(), wc, 6)]
@@ -90,9 +98,24 @@ def test_router_logits_identical_across_batch_sizes():
             assert torch.equal(a, b[:n])
 
 
+def test_router_weight_split_is_exact():
+    """plane0 + plane1 + plane2 == w exactly, for normal-range weights of
+    many magnitudes (the sum is formed in fp64, where it is exact)."""
+    g = torch.Generator().manual_seed(9)
+    w = torch.randn((64, 1024), generator=g) * torch.exp2(torch.randint(-60, 60, (64, 1), generator=g).float())
+    w[0, :8] = torch.tensor([1.0, -1.0, 3.0e38, -2.0 ** -100, 1.0 + 2.0 ** -23, 0.0, -0.0, 2.0 ** -110])
+    planes = M.moe_router_prepare(w.cuda()).cpu().float().double()
+    assert torch.equal(planes.sum(0), w.double())
+
+
 def test_router_host_errors():
-    x = torch.zeros((4, 100), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((4, 256), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((8, 100), dtype=torch.float32, device="cuda")
     with pytest.raises(M.MoeError) as e:
-        M.moe_route(x, w, 2)
+        M.moe_router_prepare(w)
     assert e.value.code == M.STATUS["MOE_ERR_UNSUPPORTED"]
+    planes = M.moe_router_prepare(torch.zeros((8, 256), dtype=torch.float32, device="cuda"))
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(M.MoeError) as e:
+        M.moe_route(x, planes, 2, ws=small)
+    assert e.value.code == M.STATUS["MOE_ERR_BUFFER_TOO_SMALL"]
