@@ -97,20 +97,31 @@ __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // one warp per expert: exclusive scan of the expert's chunk counts (which
   // become each chunk's offset inside the expert) and the expert total
+  // (up to 8 x 32 chunks of an expert are loaded together, so a warp waits
+  // for memory once per expert rather than once per 32 chunks)
+  constexpr int kLoads = 8;
   for (int ex = warp; ex < p.E_local; ex += 32) {
     int32_t* row = p.chunk_hist + static_cast<int64_t>(ex) * p.chunks;
     int carry = 0;
-    for (int c0 = 0; c0 < p.chunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = c < p.chunks ? row[c] : 0;
-      int x = v;
+    for (int c0 = 0; c0 < p.chunks; c0 += 32 * kLoads) {
+      int v[kLoads];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
+      for (int j = 0; j < kLoads; ++j) {
+        const int c = c0 + 32 * j + lane;
+        v[j] = c < p.chunks ? row[c] : 0;
       }
-      if (c < p.chunks) row[c] = carry + x - v;
-      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+#pragma unroll
+      for (int j = 0; j < kLoads; ++j) {
+        const int c = c0 + 32 * j + lane;
+        int x = v[j];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (c < p.chunks) row[c] = carry + x - v[j];
+        carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+      }
     }
     if (lane == 0) s_count[ex] = carry;
   }
