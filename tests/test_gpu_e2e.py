@@ -51,11 +51,12 @@ def test_forward_matches_oracle(case):
     assert np.all(out[~loc.any(axis=1)] == 0.0)
 
 
+@pytest.mark.parametrize("T", [97, 40])   # 40: masked max_m <= 64 takes the decode pipeline
 @pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
-def test_masked_and_compact_agree_bitwise(dtype):
-    kw = dict(T=97, K=512, I=256, E_global=32, E_local=32, topk=4, dtype=dtype, seed=11)
+def test_masked_and_compact_agree_bitwise(dtype, T):
+    kw = dict(T=T, K=512, I=256, E_global=32, E_local=32, topk=4, dtype=dtype, seed=11)
     pc = Problem(**kw, layout="compact")
-    pm = Problem(**kw, layout="masked", max_m=97)
+    pm = Problem(**kw, layout="masked", max_m=T)
     oc = pc.gpu().forward().clone()
     om = pm.gpu().forward().clone()
     assert torch.equal(oc.view(torch.int16), om.view(torch.int16))

@@ -26,6 +26,10 @@ CASES = [
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
     dict(T=600, K=512, I=256, E_global=32, E_local=32, topk=8, dtype="fp8", layout="compact", zipf_s=1.2),
+    # masked with max_m <= 64: the decode pipeline (64-row A tiles, 5 stages)
+    dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
+    dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
+    dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
     dict(T=128, K=256, I=256, E_global=8, E_local=8, topk=2, dtype="mxfp8", layout="compact"),
     dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="mxfp8", layout="compact", drop_every=5),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
