@@ -51,7 +51,7 @@ def test_forward_matches_oracle(case):
     assert np.all(out[~loc.any(axis=1)] == 0.0)
 
 
-@pytest.mark.parametrize("T", [97, 40])   # 40: masked max_m <= 64 takes the decode pipeline
+@pytest.mark.parametrize("T", [97, 40])   # 40: one partial block per masked expert
 @pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
 def test_masked_and_compact_agree_bitwise(dtype, T):
     kw = dict(T=T, K=512, I=256, E_global=32, E_local=32, topk=4, dtype=dtype, seed=11)

@@ -26,7 +26,7 @@ CASES = [
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
     dict(T=600, K=512, I=256, E_global=32, E_local=32, topk=8, dtype="fp8", layout="compact", zipf_s=1.2),
-    # masked with max_m <= 64: the decode pipeline (64-row A tiles, 5 stages)
+    # masked decode-sized blocks: max_m = 48, one partial block per expert
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
