@@ -275,10 +275,14 @@ moe_status_t moe_route(const void* x_bf16, const void* w_planes, int64_t T, int6
  * microscaling layout) into the packed order the grouped GEMMs copy into
  * tensor memory: for every (e, 128-row block, 128-column group) a 512-byte
  * chunk in which row r's four bytes (its four 32-column blocks, in column
- * order) sit at 16 * (r % 32) + 4 * (r / 32).  dst has the same size as src
- * and must not overlap it.  N and C must be multiples of 128; device
- * pointers, 16-byte aligned; enqueued on stream. */
-moe_status_t moe_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C, void* stream);
+ * order) sit at 16 * (r % 32) + 4 * (r / 32).  src_ld is the byte stride
+ * between consecutive scale rows of src: C/32, or more when the scale rows
+ * are padded (a multiple of 4) [P1 "关联脉络": padded MXFP8 scale row
+ * strides].  dst holds E * N * C/32 bytes and must not overlap src.  N and C
+ * must be multiples of 128; device pointers, 16-byte aligned; enqueued on
+ * stream. */
+moe_status_t moe_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+                                void* stream);
 
 /* Number of kernel launches one moe_forward enqueues (for launch accounting). */
 int32_t moe_forward_launches(const moe_ctx* ctx);

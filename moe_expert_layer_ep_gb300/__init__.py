@@ -92,7 +92,7 @@ def _load():
         "moe_route": (I32, [VP, VP, I64, I64, I32, I32, VP, VP, VP, VP, I64, VP]),
         "moe_route_workspace_size": (I64, [I64, I64, I32]),
         "moe_router_prepare": (I32, [VP, VP, I64, I64, VP]),
-        "moe_pack_mx_scales": (I32, [VP, VP, I64, I64, I64, VP]),
+        "moe_pack_mx_scales": (I32, [VP, I64, VP, I64, I64, I64, VP]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -341,15 +341,17 @@ def moe_route(x, w_planes, topk, logits=None, topk_ids=None, topk_weights=None, 
     return topk_ids, topk_weights, logits
 
 
-def moe_pack_mx_scales(sf, out=None, stream=None):
-    """MXFP8 weight scales uint8 [E, N, C/32] (natural layout) -> the packed
+def moe_pack_mx_scales(sf, out=None, stream=None, C=None):
+    """MXFP8 weight scales uint8 [E, N, ld] (natural layout; ld = C/32, or
+    more when the scale rows are padded, in which case pass C) -> the packed
     order moe_ctx_create takes for MOE_DTYPE_MXFP8 (see include/moe.h)."""
-    E, N, G = sf.shape
+    E, N, ld = sf.shape
+    C = ld * 32 if C is None else C
     _require_cuda("sf", sf, torch.uint8)
     if out is None:
-        out = torch.empty_like(sf)
-    _require_cuda("out", out, torch.uint8, sf.numel())
-    _check(_lib.moe_pack_mx_scales(_ptr(sf), _ptr(out), E, N, G * 32, _stream(stream)), "moe_pack_mx_scales")
+        out = torch.empty((E, N, C // 32), dtype=torch.uint8, device=sf.device)
+    _require_cuda("out", out, torch.uint8, E * N * (C // 32))
+    _check(_lib.moe_pack_mx_scales(_ptr(sf), ld, _ptr(out), E, N, C, _stream(stream)), "moe_pack_mx_scales")
     return out
 
 

@@ -469,15 +469,16 @@ moe_status_t moe_route(const void* x_bf16, const void* w_planes, int64_t T, int6
                                        static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C, void* stream) {
-  if (E < 0 || N < 0 || C < 0) return MOE_ERR_INVALID_ARG;
+moe_status_t moe_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+                                void* stream) {
+  if (E < 0 || N < 0 || C < 0 || src_ld < C / 32 || src_ld % 4) return MOE_ERR_INVALID_ARG;
   if (N % 128 || C % 128) return MOE_ERR_UNSUPPORTED;
   if (E * N * C == 0) return MOE_OK;
   if (!src || !dst) return MOE_ERR_INVALID_ARG;
   if (!aligned16(src) || !aligned16(dst)) return MOE_ERR_MISALIGNED;
-  const int64_t bytes = E * N * (C / 32);
-  if (src < dst + bytes && dst < src + bytes) return MOE_ERR_INVALID_ARG;   // overlap
-  return cuda_status(moe::launch_pack_mx_scales(src, dst, E, N, C, static_cast<cudaStream_t>(stream)));
+  const int64_t src_bytes = E * N * src_ld, dst_bytes = E * N * (C / 32);
+  if (src < dst + dst_bytes && dst < src + src_bytes) return MOE_ERR_INVALID_ARG;   // overlap
+  return cuda_status(moe::launch_pack_mx_scales(src, src_ld, dst, E, N, C, static_cast<cudaStream_t>(stream)));
 }
 
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {

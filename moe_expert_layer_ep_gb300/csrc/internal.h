@@ -91,7 +91,7 @@ cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUten
                         cudaStream_t s);
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t s);
-cudaError_t launch_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+cudaError_t launch_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,
                                   cudaStream_t s);
 struct RouterArgs {
   int64_t T, K;

@@ -84,12 +84,13 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   if (tid == 0) s_out[blk] = static_cast<uint8_t>(s + 127);
 }
 
-// MXFP8 weight scales, natural [E, N, C/32] bytes -> packed 512-byte chunks
-// per (e, 128-row block, 128-column group), row r's word at byte
-// 16 * (r % 32) + 4 * (r / 32).  A source word (4 consecutive 32-column
-// blocks of one row) is a destination word, so one thread moves one word.
-__global__ void __launch_bounds__(256) pack_mx_scales_kernel(const uint32_t* src, uint32_t* dst, int64_t words,
-                                                             int64_t N, int64_t CG) {
+// MXFP8 weight scales, natural [E, N, C/32] bytes (scale rows ld_words
+// 32-bit words apart, padded or not) -> packed 512-byte chunks per (e,
+// 128-row block, 128-column group), row r's word at byte 16 * (r % 32) +
+// 4 * (r / 32).  A source word (4 consecutive 32-column blocks of one row) is
+// a destination word, so one thread moves one word.
+__global__ void __launch_bounds__(256) pack_mx_scales_kernel(const uint32_t* src, int64_t ld_words, uint32_t* dst,
+                                                             int64_t words, int64_t N, int64_t CG) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= words) return;
   const int64_t kg = i % CG;          // 128-column group
@@ -97,17 +98,17 @@ __global__ void __launch_bounds__(256) pack_mx_scales_kernel(const uint32_t* src
   const int64_t e = i / (CG * N);
   const int r = static_cast<int>(n & 127);
   const int64_t chunk = (e * (N / 128) + (n >> 7)) * CG + kg;
-  dst[chunk * 128 + 4 * (r & 31) + (r >> 5)] = src[i];
+  dst[chunk * 128 + 4 * (r & 31) + (r >> 5)] = src[(e * N + n) * ld_words + kg];
 }
 
 }  // namespace
 
-cudaError_t launch_pack_mx_scales(const uint8_t* src, uint8_t* dst, int64_t E, int64_t N, int64_t C,
+cudaError_t launch_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,
                                   cudaStream_t st) {
   const int64_t words = E * N * (C / 128);
   if (words <= 0) return cudaSuccess;
   pack_mx_scales_kernel<<<static_cast<unsigned>((words + 255) / 256), 256, 0, st>>>(
-      reinterpret_cast<const uint32_t*>(src), reinterpret_cast<uint32_t*>(dst), words, N, C / 128);
+      reinterpret_cast<const uint32_t*>(src), src_ld / 4, reinterpret_cast<uint32_t*>(dst), words, N, C / 128);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,17 @@ def test_pack_mx_scales_layout():
     assert np.array_equal(got, want)
 
 
+def test_pack_mx_scales_padded_rows():
+    """Scale rows padded to 32 bytes (C/32 = 20 used) pack like unpadded ones."""
+    E, N, C = 2, 128, 640
+    src = torch.randint(0, 256, (E, N, C // 32), dtype=torch.uint8)
+    padded = torch.randint(0, 256, (E, N, 32), dtype=torch.uint8)
+    padded[:, :, :C // 32] = src
+    a = M.moe_pack_mx_scales(src.cuda()).cpu()
+    b = M.moe_pack_mx_scales(padded.cuda(), C=C).cpu()
+    assert torch.equal(a, b)
+
+
 def test_pack_mx_scales_host_errors():
     a = torch.zeros(2 * 128 * 4, dtype=torch.uint8, device="cuda")
     with pytest.raises(M.MoeError) as e:
