@@ -118,6 +118,38 @@ def mxfp8_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
     return w, sf
 
 
+# FP4 E2M1 magnitude codes 0..7 (0, 0.5, 1, 1.5, 2, 3, 4, 6) drawn with these
+# weights: a bell-shaped spread of codes, 6 kept rare.
+FP4_CODE_WEIGHTS = (0.10, 0.20, 0.20, 0.15, 0.13, 0.10, 0.08, 0.04)
+FP4_WEIGHT_EXPONENTS = (-9, -8)
+
+
+def mxfp4_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
+    """MXFP4 weights for experts first_expert .. first_expert+E-1, drawn as
+    codes: E2M1 codes packed two per byte (element 2j in the low nibble of
+    byte j) and one UE8M0 exponent per row and 32-column block.
+
+    Returns (w uint8 [E, N, C/2], w_sf uint8 [E, N, C/32], natural layout).
+    """
+    assert N % 128 == 0 and C % 128 == 0
+    w = torch.empty((E, N, C // 2), dtype=torch.uint8, device=device)
+    sf = torch.empty((E, N, C // 32), dtype=torch.uint8, device=device)
+    probs = torch.tensor(FP4_CODE_WEIGHTS, dtype=torch.float32, device=device)
+    rows_per_chunk = max(128, (1 << 26) // C // 128 * 128)
+    for i in range(E):
+        g = _gen(seed * 1_000_003 + first_expert + i + 104729, device)
+        choice = torch.randint(0, len(FP4_WEIGHT_EXPONENTS), (N, C // 32), generator=g, device=device)
+        sf[i] = (torch.tensor(FP4_WEIGHT_EXPONENTS, device=device)[choice] + 127).to(torch.uint8)
+        for r0 in range(0, N, rows_per_chunk):
+            r1 = min(N, r0 + rows_per_chunk)
+            n = (r1 - r0) * C
+            mag = torch.multinomial(probs, n, replacement=True, generator=g).view(r1 - r0, C)
+            sign = torch.randint(0, 2, (r1 - r0, C), generator=g, device=device) * 8
+            code = (mag + sign).to(torch.uint8)
+            w[i, r0:r1] = code[:, 0::2] | (code[:, 1::2] << 4)
+    return w, sf
+
+
 def bf16_expert_weights(E, N, C, seed, device="cpu", first_expert=0):
     """BF16 weights [E, N, C] ~ N(0, 0.02)."""
     w = torch.empty((E, N, C), dtype=torch.bfloat16, device=device)

@@ -22,7 +22,9 @@ Pinning status (what each function is checked against in ``tests/``):
   exhaustive bf16 sweeps; UE8M0 exponent against a brute-force search;
   1x32 (MXFP8) groups against torch's e4m3 cast with a brute-force minimal
   exponent, against the 1x128 routine on tiled blocks, and equal to 1x128
-  where the four blocks of a group share their exponent.
+  where the four blocks of a group share their exponent; E2M1 (FP4) values
+  against the E4M3 grid (pinned above): exactly the E4M3 values of at most
+  two significant bits between 0.5 and 6, plus zero.
 * ``layout``: the static compact bound against brute force over every
   routing of tiny problems; plan invariants (bijection, stability, ``-1``
   padding) on random routings.
@@ -51,6 +53,8 @@ from .formats import (  # noqa: F401
     quant_fp8_groups,
     dequant_groups,
     quant_mxfp8_1x32,
+    e2m1_from_codes,
+    unpack_fp4,
 )
 from .layout import (  # noqa: F401
     compact_all_tokens,
@@ -61,6 +65,7 @@ from .moe import (  # noqa: F401
     combine,
     dequant_fp8_weights,
     dequant_mx_weights,
+    dequant_mxfp4_weights,
     expert_ffn,
     gemm1_act,
     gemm2,

@@ -20,7 +20,10 @@ that final scale before rounding to E4M3.
 MXFP8 (the 1x32 variant, which the standard-dispatch report lists as not yet
 covered, section "风险与影响" item 5) is read as the same element format and
 the same exponent rule over 32-column blocks (the OCP microscaling block
-size), for activations, the GEMM1 output and each weight row.
+size), for activations, the GEMM1 output and each weight row.  The FP4
+variant of the same item is read as FP4 (E2M1) expert weights with one UE8M0
+scale per row and 32-column block (OCP MXFP4), the activations and h staying
+MXFP8.
 """
 
 import math
@@ -144,6 +147,28 @@ def quant_mxfp8_1x32(x):
     exponent follows the layer's rule (smallest s with amax <= 448 * 2^s),
     applied per 32-column block: ``quant_fp8_groups(x, 32)``."""
     return quant_fp8_groups(x, 32)
+
+
+def e2m1_from_codes(codes):
+    """FP4 E2M1 (the OCP microscaling FP4 element: 1 sign, 2 exponent bits with
+    bias 1, 1 mantissa bit, subnormals, no inf / NaN) codes 0..15 -> fp64.
+    Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6."""
+    c = np.asarray(codes, dtype=np.int64)
+    sign = np.where(c & 8, -1.0, 1.0)
+    ef = (c >> 1) & 3
+    mf = c & 1
+    mag = np.where(ef == 0, 0.5 * mf, np.ldexp(1.0 + 0.5 * mf, ef - 1))
+    return sign * mag
+
+
+def unpack_fp4(packed):
+    """uint8 [..., C/2] -> codes [..., C]: element 2j in the low nibble of byte
+    j, element 2j + 1 in the high nibble."""
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int64)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
 
 
 def exp2i(s):

@@ -26,6 +26,8 @@ Readings adopted where the reports are silent:
 * MXFP8 (dtype "mxfp8"): every scale covers 1x32 instead -- activations and
   h per row and 32-column block, weights per row and 32-column block along
   the reduction dimension -- with the same exponent rule.
+* MXFP4 (dtype "mxfp4"): the weights are FP4 E2M1 with 1x32 UE8M0 scales;
+  activations and h are MXFP8.
 
 All sums are fp64.  ``forward_layout`` follows the layout path;
 ``forward_per_token`` computes the same layer one token at a time with no
@@ -34,7 +36,8 @@ layout at all, and the two must agree bitwise.
 
 import numpy as np
 
-from .formats import bf16_round, dequant_1x128, dequant_groups, e4m3_from_bits, quant_fp8_1x128, quant_mxfp8_1x32
+from .formats import (bf16_round, dequant_1x128, dequant_groups, e2m1_from_codes, e4m3_from_bits, quant_fp8_1x128,
+                      quant_mxfp8_1x32, unpack_fp4)
 from .layout import plan_layout, use_masked_layout
 
 
@@ -63,13 +66,23 @@ def dequant_mx_weights(w_bytes, w_exp):
     return (w.reshape(E, N, C // 32, 32) * scale[..., None]).reshape(E, N, C)
 
 
+def dequant_mxfp4_weights(w_packed, w_exp):
+    """MXFP4 weights: E2M1 codes packed two per byte, [E, N, C/2] (element 2j
+    in the low nibble of byte j), with one exponent per row and 32-column
+    block, [E, N, C/32] -> fp64 values [E, N, C]."""
+    w = e2m1_from_codes(unpack_fp4(w_packed))
+    E, N, C = w.shape
+    scale = np.ldexp(1.0, np.asarray(w_exp, dtype=np.int64))   # [E, N, C/32]
+    return (w.reshape(E, N, C // 32, 32) * scale[..., None]).reshape(E, N, C)
+
+
 def store_act(x, dtype):
     """Quantise activation rows to the GEMM input format; returns the fp64
     values the GEMM consumes and, for FP8 / MXFP8, the (q, s) pair."""
     if dtype == "fp8":
         q, s = quant_fp8_1x128(x)
         return dequant_1x128(q, s), (q, s)
-    if dtype == "mxfp8":
+    if dtype in ("mxfp8", "mxfp4"):          # MXFP4 weights keep MXFP8 activations
         q, s = quant_mxfp8_1x32(x)
         return dequant_groups(q, s, 32), (q, s)
     if dtype == "bf16":
@@ -136,7 +149,7 @@ def forward_layout(x, w13, w2, topk_ids, topk_weights, dtype, E_global, expert_s
 
     x [T, K] fp64 (bf16 values); w13 [E_local, 2I, K], w2 [E_local, K, I]
     fp64 (dequantised weights); topk_ids int [T, k]; topk_weights [T, k]
-    (fp32 values).  dtype "fp8", "mxfp8" or "bf16".  Returns out [T, K] (bf16 values)
+    (fp32 values).  dtype "fp8", "mxfp8", "mxfp4" or "bf16".  Returns out [T, K] (bf16 values)
     and, with keep=True, a dict with the plan and every stored intermediate.
     """
     x = np.asarray(x, dtype=np.float64)
