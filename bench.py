@@ -151,9 +151,10 @@ def build_inputs(w, device):
     if w["dtype"] == "fp8":
         w13, w13s = synth.fp8_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
         w2, w2s = synth.fp8_expert_weights(w["E_local"], K, I, w["seed"] + 3, device, es)
-    elif w["dtype"] == "mxfp8":      # natural [E, N, C/32] scales (packed for the device by run_ours)
-        w13, w13s = synth.mxfp8_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
-        w2, w2s = synth.mxfp8_expert_weights(w["E_local"], K, I, w["seed"] + 3, device, es)
+    elif w["dtype"] in ("mxfp8", "mxfp4"):   # natural [E, N, C/32] scales (packed for the device by run_ours)
+        gen = synth.mxfp8_expert_weights if w["dtype"] == "mxfp8" else synth.mxfp4_expert_weights
+        w13, w13s = gen(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
+        w2, w2s = gen(w["E_local"], K, I, w["seed"] + 3, device, es)
     else:
         w13 = synth.bf16_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
         w2 = synth.bf16_expert_weights(w["E_local"], K, I, w["seed"] + 3, device, es)
@@ -168,11 +169,12 @@ def work_model(w, ids):
     loc = (ids >= es) & (ids < es + E_l)
     A = int(loc.sum())
     nonempty = len(np.unique(ids[loc]))
-    esz = 1 if w["dtype"] in ("fp8", "mxfp8") else 2
+    esz = 1 if w["dtype"] in ("fp8", "mxfp8", "mxfp4") else 2    # activations and h
+    wsz = 0.5 if w["dtype"] == "mxfp4" else esz                   # weights
     flops1 = 2.0 * A * K * 2 * I
     flops2 = 2.0 * A * I * K
-    w13_bytes = nonempty * 2 * I * K * esz
-    w2_bytes = nonempty * K * I * esz
+    w13_bytes = nonempty * 2 * I * K * wsz
+    w2_bytes = nonempty * K * I * wsz
     # GEMM1 reads its weights, the valid a rows, writes h; GEMM2 likewise.
     g1_bytes = w13_bytes + A * K * esz + A * I * esz
     g2_bytes = w2_bytes + A * I * esz + A * K * 2
@@ -198,8 +200,9 @@ class OracleRunner:
     def expert(self, e):
         if e not in self.cache:
             w13, w13s, w2, w2s = self.weights
-            if self.w["dtype"] in ("fp8", "mxfp8"):
-                deq = self.oracle.dequant_fp8_weights if self.w["dtype"] == "fp8" else self.oracle.dequant_mx_weights
+            if self.w["dtype"] in ("fp8", "mxfp8", "mxfp4"):
+                deq = {"fp8": self.oracle.dequant_fp8_weights, "mxfp8": self.oracle.dequant_mx_weights,
+                       "mxfp4": self.oracle.dequant_mxfp4_weights}[self.w["dtype"]]
                 a = deq(w13[e:e + 1].numpy(), w13s[e:e + 1].numpy().astype(np.int64) - 127)[0]
                 b = deq(w2[e:e + 1].numpy(), w2s[e:e + 1].numpy().astype(np.int64) - 127)[0]
             else:
@@ -262,7 +265,7 @@ def run_ours(args, w, world, rank, local):
     shape = M.make_shape(w["T"], w["K"], w["I"], w["E_global"], w["E_local"], w["topk"], w["dtype"], w["layout"],
                          w["expert_start"], w.get("max_m", 0) or (w["T"] if w["layout"] == "masked" else 0))
     ctx_weights = weights
-    if w["dtype"] == "mxfp8":      # the context takes packed MX scales; the oracle reads the natural ones
+    if w["dtype"] in ("mxfp8", "mxfp4"):   # the context takes packed MX scales; the oracle reads the natural ones
         ctx_weights = (weights[0], M.moe_pack_mx_scales(weights[1]), weights[2], M.moe_pack_mx_scales(weights[3]))
     ctx = M.moe_ctx_create(shape, *ctx_weights)
     ws = M.alloc_workspace(ctx, dev)
@@ -374,7 +377,7 @@ def run_ours(args, w, world, rank, local):
     med = np.median(stage_ms, axis=0)
     g1_ms, g2_ms = float(med[2]), float(med[3])
     gemm_tflops = (wm["flops1"] + wm["flops2"]) / ((g1_ms + g2_ms) / 1000.0) / 1e12
-    fp8 = w["dtype"] in ("fp8", "mxfp8")
+    fp8 = w["dtype"] in ("fp8", "mxfp8", "mxfp4")
     tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     g1_gbs = wm["g1_bytes"] / (g1_ms / 1000.0) / 1e9
     g1_tf = wm["flops1"] / (g1_ms / 1000.0) / 1e12
@@ -396,7 +399,8 @@ def run_ours(args, w, world, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": {"fp8": "fp8-e4m3/ue8m0", "mxfp8": "mxfp8-e4m3/ue8m0-1x32"}.get(w["dtype"], "bf16"),
+        "scaling": "weak", "vs_baseline": None, "dtype": {"fp8": "fp8-e4m3/ue8m0", "mxfp8": "mxfp8-e4m3/ue8m0-1x32",
+                  "mxfp4": "mxfp4-e2m1-weights/mxfp8-activations"}.get(w["dtype"], "bf16"),
         "data": "synthetic (seeded; random-init weights)",
         "config": {"workload": w["name"], "T": T, "K": w["K"], "I": w["I"], "E": w["E_local"],
                    "topk": w["topk"], "layout": w["layout"], "l2": "weights larger than L2 (no flush needed)",

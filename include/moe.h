@@ -59,8 +59,10 @@ typedef enum {
 typedef enum {
   MOE_DTYPE_FP8_E4M3_UE8M0 = 0, /* FP8 e4m3 operands, UE8M0 scales: 1x128 (activations), 128x128 (weights) */
   MOE_DTYPE_BF16 = 1,           /* bf16 operands, no scales */
-  MOE_DTYPE_MXFP8 = 2           /* FP8 e4m3 operands, one UE8M0 scale per 1x32 block for activations, h
+  MOE_DTYPE_MXFP8 = 2,          /* FP8 e4m3 operands, one UE8M0 scale per 1x32 block for activations, h
                                    and every weight row (the MXFP8 variant [P1 "风险与影响" 5]) */
+  MOE_DTYPE_MXFP4 = 3           /* FP4 E2M1 weights with one UE8M0 scale per row and 1x32 block (MXFP4),
+                                   activations and h as for MXFP8 (the FP4 variant [P1 "风险与影响" 5]) */
 } moe_dtype_t;
 
 /* Row layout of the expert inputs [P1 "实现拆解" 2, "关键源码片段" deep_gemm.py]. */
@@ -134,12 +136,15 @@ int32_t moe_choose_layout(int32_t E_global, int32_t E_local);
  *   MXFP8: w13, w2 as for FP8; w13_sf / w2_sf hold one UE8M0 byte per row and
  *         32-column block ([E_local, 2I, K/32] / [E_local, K, I/32]) in the
  *         packed order moe_pack_mx_scales writes (16-byte aligned)
+ *   MXFP4: w13 uint8 [E_local, 2I, K/2], w2 uint8 [E_local, K, I/2]: E2M1 codes,
+ *         two per byte, element 2j in the low nibble of byte j; scales as
+ *         for MXFP8
  *   BF16: w13 bf16 [E_local, 2I, K], w2 bf16 [E_local, K, I]; w13_sf = w2_sf = NULL
  * Rows 0..I-1 of w13[e] are the gate projection W1, rows I..2I-1 the up
  * projection W3 [P2 "关键源码片段" deep_gemm.py: the activation splits the
  * GEMM output in halves].  Weights are read, never written, and must stay
  * alive while the context is used.  A scale pointer given for BF16 or missing
- * for FP8 / MXFP8 is MOE_ERR_DTYPE_MISMATCH.  Host-only: builds the weight TMA
+ * for FP8 / MXFP8 / MXFP4 is MOE_ERR_DTYPE_MISMATCH.  Host-only: builds the weight TMA
  * descriptors; allocates no device memory. */
 moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uint8_t* w13_sf,
                             const void* w2, const uint8_t* w2_sf, moe_ctx** out);

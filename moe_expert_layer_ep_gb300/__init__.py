@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 MOE_DTYPE_FP8 = 0
 MOE_DTYPE_BF16 = 1
 MOE_DTYPE_MXFP8 = 2
+MOE_DTYPE_MXFP4 = 3
 MOE_LAYOUT_AUTO = 0
 MOE_LAYOUT_COMPACT = 1
 MOE_LAYOUT_MASKED = 2
@@ -163,11 +164,12 @@ class MoeContext:
     @property
     def fp8(self):
         """FP8 operands (1x128 / 128x128 or MXFP8 1x32 scales)."""
-        return self.shape.dtype in (MOE_DTYPE_FP8, MOE_DTYPE_MXFP8)
+        return self.shape.dtype in (MOE_DTYPE_FP8, MOE_DTYPE_MXFP8, MOE_DTYPE_MXFP4)
 
     @property
     def mx(self):
-        return self.shape.dtype == MOE_DTYPE_MXFP8
+        """1x32 scales on activations and h (MXFP8 and MXFP4)."""
+        return self.shape.dtype in (MOE_DTYPE_MXFP8, MOE_DTYPE_MXFP4)
 
     @property
     def masked(self):
@@ -182,7 +184,7 @@ class MoeContext:
 def make_shape(T, K, I, E_global, E_local, topk, dtype, layout=MOE_LAYOUT_AUTO, expert_start=0, max_m=0,
                block_e=128):
     if isinstance(dtype, str):
-        dtype = {"fp8": MOE_DTYPE_FP8, "bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8}[dtype]
+        dtype = {"fp8": MOE_DTYPE_FP8, "bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8, "mxfp4": MOE_DTYPE_MXFP4}[dtype]
     if isinstance(layout, str):
         layout = {"auto": MOE_LAYOUT_AUTO, "compact": MOE_LAYOUT_COMPACT, "masked": MOE_LAYOUT_MASKED}[layout]
     return MoeShape(T=T, K=K, I=I, E_global=E_global, E_local=E_local, expert_start=expert_start, topk=topk,
@@ -191,12 +193,14 @@ def make_shape(T, K, I, E_global, E_local, topk, dtype, layout=MOE_LAYOUT_AUTO, 
 
 def moe_ctx_create(shape, w13, w13_sf, w2, w2_sf):
     """shape: MoeShape; weights as in include/moe.h (CUDA tensors)."""
-    mx = shape.dtype == MOE_DTYPE_MXFP8
+    fp4 = shape.dtype == MOE_DTYPE_MXFP4
+    mx = shape.dtype == MOE_DTYPE_MXFP8 or fp4
     fp8 = shape.dtype == MOE_DTYPE_FP8 or mx
     E, K, I = shape.E_local, shape.K, shape.I
     wdt = torch.uint8 if fp8 else torch.bfloat16
-    _require_cuda("w13", w13, wdt, E * 2 * I * K)
-    _require_cuda("w2", w2, wdt, E * K * I)
+    wd = 2 if fp4 else 1      # two FP4 codes per byte
+    _require_cuda("w13", w13, wdt, E * 2 * I * K // wd)
+    _require_cuda("w2", w2, wdt, E * K * I // wd)
     if w13_sf is not None:
         _require_cuda("w13_sf", w13_sf, torch.uint8, E * 2 * I * K // 32 if mx else E * (2 * I // 128) * (K // 128))
     if w2_sf is not None:

@@ -16,7 +16,8 @@ struct moe_ctx {
   moe_shape_t shape;
   int layout;  // resolved: MOE_LAYOUT_COMPACT or MOE_LAYOUT_MASKED
   bool fp8;   // FP8 operands (1x128 / 128x128 or MXFP8 scales)
-  bool mx;    // MXFP8: 1x32 scales
+  bool mx;    // MXFP8 / MXFP4: 1x32 scales
+  bool fp4;   // MXFP4: FP4 (E2M1) weights
   const void* w13;
   const uint8_t* w13_sf;
   const void* w2;
@@ -58,18 +59,21 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // 3-D K-major tile map over [dim2][dim1][dim0] with a 128-byte inner box and
 // 128 rows, 128-byte swizzle (the layout the MMA descriptors expect).
-moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2) {
+// packed4: byte rows of packed FP4 codes, a 64-byte inner box, no swizzle
+// (the kernel expands them into the swizzled e4m3 layout itself).
+moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                      bool packed4 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
   const uint64_t esize = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
   cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>((packed4 ? 64 : 128) / esize), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  packed4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -79,7 +83,8 @@ moe_status_t check_shape(const moe_shape_t* s) {
       s->topk <= 0)
     return MOE_ERR_INVALID_ARG;
   if (static_cast<int64_t>(s->E_local) + s->expert_start > s->E_global) return MOE_ERR_INVALID_ARG;
-  if (s->dtype != MOE_DTYPE_FP8_E4M3_UE8M0 && s->dtype != MOE_DTYPE_BF16 && s->dtype != MOE_DTYPE_MXFP8)
+  if (s->dtype != MOE_DTYPE_FP8_E4M3_UE8M0 && s->dtype != MOE_DTYPE_BF16 && s->dtype != MOE_DTYPE_MXFP8 &&
+      s->dtype != MOE_DTYPE_MXFP4)
     return MOE_ERR_INVALID_ARG;
   if (s->layout != MOE_LAYOUT_AUTO && s->layout != MOE_LAYOUT_COMPACT && s->layout != MOE_LAYOUT_MASKED)
     return MOE_ERR_INVALID_ARG;
@@ -172,6 +177,7 @@ moe::GemmArgs gemm_args(const moe_ctx* c, void* ws, int stage) {
   g.stage = stage;
   g.fp8 = c->fp8;
   g.mx = c->mx;
+  g.fp4 = c->fp4;
   g.masked = c->layout == MOE_LAYOUT_MASKED;
   g.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
   const int64_t red = stage == 1 ? s.K : s.I;
@@ -223,7 +229,8 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   *out = nullptr;
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
-  const bool mx = shape->dtype == MOE_DTYPE_MXFP8;
+  const bool fp4 = shape->dtype == MOE_DTYPE_MXFP4;
+  const bool mx = shape->dtype == MOE_DTYPE_MXFP8 || fp4;
   const bool fp8 = shape->dtype == MOE_DTYPE_FP8_E4M3_UE8M0 || mx;
   if (!w13 || !w2) return MOE_ERR_INVALID_ARG;
   if (fp8 != (w13_sf != nullptr) || fp8 != (w2_sf != nullptr)) return MOE_ERR_DTYPE_MISMATCH;
@@ -242,6 +249,7 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   c->layout = layout;
   c->fp8 = fp8;
   c->mx = mx;
+  c->fp4 = fp4;
   c->w13 = w13;
   c->w13_sf = w13_sf;
   c->w2 = w2;
@@ -253,8 +261,9 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
     return MOE_ERR_CUDA;
   }
   compute_ws_layout(c);
-  st = make_map(&c->map_w13, w13, fp8, shape->K, 2 * shape->I, shape->E_local);
-  if (st == MOE_OK) st = make_map(&c->map_w2, w2, fp8, shape->I, shape->K, shape->E_local);
+  const int64_t wd = fp4 ? 2 : 1;   // MXFP4: two codes per byte along K
+  st = make_map(&c->map_w13, w13, fp8, shape->K / wd, 2 * shape->I, shape->E_local, fp4);
+  if (st == MOE_OK) st = make_map(&c->map_w2, w2, fp8, shape->I / wd, shape->K, shape->E_local, fp4);
   if (st != MOE_OK) {
     delete c;
     return st;

@@ -51,35 +51,65 @@ namespace moe {
 
 namespace {
 
-constexpr int kStages = 4;
 // Epilogue warps per (dtype, stage).  The FP8 GEMM1 epilogue (one
 // accumulator: its other tensor-memory columns hold the scale tiles) uses 8,
 // two per accumulator lane quadrant with half of the columns each, copies the
 // accumulator out and releases it before the activation and quantisation.
 // The others use 4 warps that interleave tensor-memory loads and stores
 // chunk by chunk (measured faster there).
-__host__ __device__ constexpr int epi_warps(bool fp8, int stage) { return (fp8 && stage == 1) ? 8 : 4; }
-__host__ __device__ constexpr int threads_for(bool fp8, int stage) { return 64 + 32 * epi_warps(fp8, stage); }
+// MXFP4 weights: GEMM1 keeps 4 epilogue warps (each 32-column chunk is one
+// 1x32 scale group, so no amax exchange is needed) and the registers go to
+// 4 warps that expand the FP4 weights to e4m3 in shared memory.
+__host__ __device__ constexpr int epi_warps(bool fp8, int stage, bool fp4 = false) {
+  return (fp8 && stage == 1 && !fp4) ? 8 : 4;
+}
+constexpr int kConvWarps = 4;
+__host__ __device__ constexpr int threads_for(bool fp8, int stage, bool fp4) {
+  return 64 + 32 * epi_warps(fp8, stage, fp4) + (fp4 ? 32 * kConvWarps : 0);
+}
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kKBlockBytes = 128;                  // one 128-byte swizzle atom of K per stage
 constexpr int kABytes = kTileM * kKBlockBytes;     // 16 KB
 constexpr int kBBytes = kTileN * kKBlockBytes;     // 32 KB
+constexpr int kBPBytes = kTileN * kKBlockBytes / 2;   // MXFP4: the packed B tile, 16 KB
 constexpr int kSfaBytes = 512;
 constexpr int kSfbBytes = 1024;
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kABytes;
-constexpr int kOffSfa = kOffB + kStages * kBBytes;
-constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
-constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 4;   // ... + per-quadrant amax exchange
-constexpr int kOffHolder = kOffBar + kNumBars * 8;
-constexpr int kOffAbort = kOffHolder + 8;
-constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
-constexpr int kSmemUsed = kOffAmax + 2 * 4 * 2 * 32 * 4;
-constexpr int kSmemBytes = kSmemUsed + 1024;       // slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;               // FP8: scale tiles live in columns 256..383
+
+// Shared-memory map.  MXFP4 weights add a packed B buffer per stage, so 3
+// stages fit instead of 4.
+template <bool kFP4>
+struct Lay {
+  static constexpr int kStages = kFP4 ? 3 : 4;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffBP = kOffB + kStages * kBBytes;
+  static constexpr int kOffSfa = kOffBP + (kFP4 ? kStages * kBPBytes : 0);
+  static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
+  static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4;   // full, empty, conv; acc; done; amax exchange
+  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffHolder + 8;
+  static constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
+  static constexpr int kSmemBytes = kOffAmax + 2 * 4 * 2 * 32 * 4 + 1024;   // + 1024-byte alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// Eight E2M1 codes (one 32-bit word, element order from the low nibble) ->
+// eight e4m3 bytes (*lo: elements 0..3, *hi: 4..7).  The magnitudes 0, 0.5,
+// 1, 1.5, 2, 3, 4, 6 are e4m3 0x00 0x30 0x38 0x3C 0x40 0x44 0x48 0x4C, picked
+// with a byte permute on the low three bits of each nibble.  The sign: a
+// nibble with bit 3 set becomes selector 12 (sign-replicate of a 0x80 byte,
+// i.e. 0xFF), one without becomes 0 (a zero byte); masked to bit 7.  Exact:
+// every E2M1 value is an e4m3 value.
+__device__ __forceinline__ void fp4x8_to_e4m3(uint32_t w, uint32_t* lo, uint32_t* hi) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t sg = (w & 0x88888888u) | ((w >> 1) & 0x44444444u);
+  *lo = __byte_perm(0x3C383000u, 0x4C484440u, m) | (__byte_perm(0u, 0x80u, sg) & 0x80808080u);
+  *hi = __byte_perm(0x3C383000u, 0x4C484440u, m >> 16) | (__byte_perm(0u, 0x80u, sg >> 16) & 0x80808080u);
+}
 
 // Instruction descriptors (M = 128, N = 256, both operands K-major, fp32 D).
 constexpr uint32_t kIdescBF16 = (1u << 4)      // D format f32
@@ -129,10 +159,14 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
 
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
-template <bool kFP8, bool kMX, int kStage>
-__global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
+template <bool kFP8, bool kMX, int kStage, bool kFP4>
+__global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const GemmArgs g) {
+  using L = Lay<kFP4>;
+  constexpr int kStages = L::kStages;
+  constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffBP = L::kOffBP, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
+  constexpr int kOffBar = L::kOffBar, kOffHolder = L::kOffHolder, kOffAbort = L::kOffAbort, kOffAmax = L::kOffAmax;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -143,6 +177,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint64_t* done = bars + 2 * kStages + 4;
   uint64_t* xchg = bars + 2 * kStages + 5;  // [4]: the two epilogue warps of a lane quadrant
+  uint64_t* conv = bars + 2 * kStages + 9;  // [kStages] MXFP4: B expanded to e4m3
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kOffHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
@@ -155,10 +190,12 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage));
+      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage, kFP4));
     }
     mbar_init(done, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&xchg[q], 64);
+    if (kFP4)
+      for (int s = 0; s < kStages; ++s) mbar_init(&conv[s], 32 * kConvWarps);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
@@ -222,12 +259,20 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
           __syncwarp();
         }
         if (lane == 0) {
-          const uint32_t bytes = kABytes + kBBytes + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
+          const uint32_t bytes =
+              kABytes + (kFP4 ? kBPBytes : kBBytes) + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kc = kb * kElemsPerKBlock;
           tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
-          tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, &full[stage], kc, r0, tl.expert);
-          tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, &full[stage], kc, r1, tl.expert);
+          if (kFP4) {
+            // packed E2M1 rows, 64 bytes per row per K block, unswizzled
+            tma_load_3d(smem + kOffBP + stage * kBPBytes, &map_b, &full[stage], kc / 2, r0, tl.expert);
+            tma_load_3d(smem + kOffBP + stage * kBPBytes + kBPBytes / 2, &map_b, &full[stage], kc / 2, r1,
+                        tl.expert);
+          } else {
+            tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, &full[stage], kc, r0, tl.expert);
+            tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, &full[stage], kc, r1, tl.expert);
+          }
           if (kFP8) {
             bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + sf_chunk_offset(tl.sf_block, kb, k_blocks),
                       kSfaBytes, &full[stage]);
@@ -282,7 +327,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTileN);
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, g.timeout_ns)) {
+          // MXFP4: the converter warps signal once B is e4m3 (after the TMA landed)
+          if (!mbar_wait_bounded(kFP4 ? &conv[stage] : &full[stage], phase, abort_flag, g.timeout_ns)) {
             ok = false;
             break;
           }
@@ -327,13 +373,52 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
       const int never = 0;
       mbar_wait_bounded(done, 0, &never, g.timeout_ns);
     }
+  } else if (kFP4 && warp >= 2 + epi_warps(kFP8, kStage, kFP4)) {
+    // ------------------------------------------------------------------ FP4 -> e4m3
+    // Each stage's packed B tile (256 rows x 64 bytes) becomes the e4m3 B
+    // tile (two 128-row boxes of 128-byte rows, 128-byte swizzle: 16-byte
+    // chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16)).
+    const int ct = threadIdx.x - 32 * (2 + epi_warps(kFP8, kStage, kFP4));
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        const bool got = mbar_wait_bounded(&full[stage], phase, abort_flag, g.timeout_ns);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* src = smem + kOffBP + stage * kBPBytes;
+        uint8_t* dst = smem + kOffB + stage * kBBytes;
+#pragma unroll 4
+        for (int q = ct; q < kTileN * 8; q += 32 * kConvWarps) {
+          const int row = q >> 3, c = q & 7;
+          const uint2 pk = *reinterpret_cast<const uint2*>(src + row * 64 + c * 8);
+          uint4 o;
+          fp4x8_to_e4m3(pk.x, &o.x, &o.y);
+          fp4x8_to_e4m3(pk.y, &o.z, &o.w);
+          *reinterpret_cast<uint4*>(dst + (row >> 7) * (kBBytes / 2) + (row & 127) * 128 + ((c ^ (row & 7)) << 4)) = o;
+        }
+        fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor cores
+        mbar_arrive(&conv[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok) {
+      set_status(g.status, MOE_ERR_TIMEOUT);
+      *abort_flag = 1;
+    }
   } else {
     // ------------------------------------------------------------------ epilogue
     // Eight warps: two per tensor-memory lane quadrant (warp % 4), each
     // owning half of the tile's columns.  A thread copies its accumulator
     // slice to registers and releases the accumulator before any math, so
     // the next tile's MMAs never wait on activation, quantisation or stores.
-    constexpr int kEpiWarps = epi_warps(kFP8, kStage);
+    constexpr int kEpiWarps = epi_warps(kFP8, kStage, kFP4);
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;  // 0 when there are four epilogue warps
     const int r = quad * 32 + lane;
@@ -355,7 +440,50 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
       const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kTileN) + (static_cast<uint32_t>(quad * 32) << 16);
       const bool row_ok = r < tl.valid;
       const int64_t row = tl.row0 + r;
-      if (kStage == 1 && kEpiWarps == 4) {
+      if (kStage == 1 && kEpiWarps == 4 && kFP8) {
+        // MXFP4 weights: h in MXFP8, each 32-column chunk one scale group
+        uint8_t* dst = static_cast<uint8_t*>(g.out) + row * g.out_ld + tl.nb * 128;
+        uint32_t sfw = 0;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t gv[32], uv[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, gv);
+          tmem_ld_32x32b_x32(taddr + 128 + c * 32, uv);
+          tmem_ld_wait();
+          if (c == 3) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          float h[32];
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            h[i] = silu_mul(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
+            amax = fmaxf(amax, fabsf(h[i]));
+          }
+          const int s = ue8m0_exponent(amax);
+          const float mul = exp2_neg(s);
+          sfw |= static_cast<uint32_t>(s + 127) << (8 * c);
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+              const int b = 16 * v;
+              uint4 o;
+              o.x = cvt_e4m3x2(h[b + 0] * mul, h[b + 1] * mul) | (cvt_e4m3x2(h[b + 2] * mul, h[b + 3] * mul) << 16);
+              o.y = cvt_e4m3x2(h[b + 4] * mul, h[b + 5] * mul) | (cvt_e4m3x2(h[b + 6] * mul, h[b + 7] * mul) << 16);
+              o.z = cvt_e4m3x2(h[b + 8] * mul, h[b + 9] * mul) |
+                    (cvt_e4m3x2(h[b + 10] * mul, h[b + 11] * mul) << 16);
+              o.w = cvt_e4m3x2(h[b + 12] * mul, h[b + 13] * mul) |
+                    (cvt_e4m3x2(h[b + 14] * mul, h[b + 15] * mul) << 16);
+              d4[v] = o;
+            }
+          }
+        }
+        if (row_ok)
+          *reinterpret_cast<uint32_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
+                                       sf_row_offset(r)) = sfw;
+      } else if (kStage == 1 && kEpiWarps == 4) {
         uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -511,16 +639,17 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage), 1)
   }
 }
 
-template <bool kFP8, bool kMX, int kStage>
+template <bool kFP8, bool kMX, int kStage, bool kFP4 = false>
 cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
+  constexpr int kSmemBytes = Lay<kFP4>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kMX, kStage><<<grid, threads_for(kFP8, kStage), kSmemBytes, s>>>(a, b, g);
+  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4><<<grid, threads_for(kFP8, kStage, kFP4), kSmemBytes, s>>>(a, b, g);
   return cudaGetLastError();
 }
 
@@ -541,9 +670,13 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 
 }  // namespace
 
-int gemm_smem_bytes(int) { return kSmemBytes; }
+int gemm_smem_bytes(int fp4) { return fp4 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
+  if (g.fp4) {
+    return g.stage == 1 ? launch_one<true, true, 1, true>(g, a, b, grid, s)
+                        : launch_one<true, true, 2, true>(g, a, b, grid, s);
+  }
   if (g.mx) {
     return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, grid, s) : launch_one<true, true, 2>(g, a, b, grid, s);
   }

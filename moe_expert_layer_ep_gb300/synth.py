@@ -194,4 +194,9 @@ WORKLOADS = {
                                dtype="mxfp8", layout="compact", zipf_s=1.2, seed=0x4D6F45_0003),
     "mxfp8_masked_decode": dict(T=64, K=7168, I=2048, E_global=256, E_local=32, expert_start=0, topk=8,
                                 dtype="mxfp8", layout="masked", zipf_s=None, seed=0x4D6F45_0003),
+    # FP4 (E2M1) weights with 1x32 UE8M0 scales, MXFP8 activations
+    "mxfp4_prefill_zipf": dict(T=8192, K=7168, I=2048, E_global=256, E_local=256, expert_start=0, topk=8,
+                               dtype="mxfp4", layout="compact", zipf_s=1.2, seed=0x4D6F45_0003),
+    "mxfp4_masked_decode": dict(T=64, K=7168, I=2048, E_global=256, E_local=32, expert_start=0, topk=8,
+                                dtype="mxfp4", layout="masked", zipf_s=None, seed=0x4D6F45_0003),
 }

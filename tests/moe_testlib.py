@@ -43,6 +43,10 @@ class Problem:
         if dtype == "fp8":
             self.w13, self.w13_sf = synth.fp8_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
             self.w2, self.w2_sf = synth.fp8_expert_weights(E_local, K, I, ws + 1, weight_device, expert_start)
+        elif dtype == "mxfp4":
+            # packed E2M1 codes + natural [E, N, C/32] scales; GpuLayer packs the scales
+            self.w13, self.w13_sf = synth.mxfp4_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
+            self.w2, self.w2_sf = synth.mxfp4_expert_weights(E_local, K, I, ws + 1, weight_device, expert_start)
         elif dtype == "mxfp8":
             # natural [E, N, C/32] scale layout; GpuLayer packs it for the device
             self.w13, self.w13_sf = synth.mxfp8_expert_weights(E_local, 2 * I, K, ws, weight_device, expert_start)
@@ -60,8 +64,9 @@ class Problem:
     def expert_weights64(self, e):
         """fp64 dequantised (w13[e], w2[e]) for local expert e (cached)."""
         if e not in self._deq:
-            if self.dtype in ("fp8", "mxfp8"):
-                deq = oracle.dequant_fp8_weights if self.dtype == "fp8" else oracle.dequant_mx_weights
+            if self.dtype in ("fp8", "mxfp8", "mxfp4"):
+                deq = {"fp8": oracle.dequant_fp8_weights, "mxfp8": oracle.dequant_mx_weights,
+                       "mxfp4": oracle.dequant_mxfp4_weights}[self.dtype]
                 w13 = deq(self.w13[e:e + 1].cpu().numpy(), self.w13_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
                 w2 = deq(self.w2[e:e + 1].cpu().numpy(), self.w2_sf[e:e + 1].cpu().numpy().astype(np.int64) - 127)[0]
             else:
@@ -122,7 +127,7 @@ class GpuLayer:
         self.w2 = p.w2.to(dev)
         self.w13_sf = None if p.w13_sf is None else p.w13_sf.to(dev)
         self.w2_sf = None if p.w2_sf is None else p.w2_sf.to(dev)
-        if p.dtype == "mxfp8":
+        if p.dtype in ("mxfp8", "mxfp4"):
             self.w13_sf = M.moe_pack_mx_scales(self.w13_sf)
             self.w2_sf = M.moe_pack_mx_scales(self.w2_sf)
         self.ctx = M.moe_ctx_create(self.shape, self.w13, self.w13_sf, self.w2, self.w2_sf)

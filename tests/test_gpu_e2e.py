@@ -29,6 +29,8 @@ SMALL = [
     dict(T=40, K=256, I=128, E_global=40, E_local=20, topk=3, dtype="fp8", layout="compact", expert_start=20),
     dict(T=333, K=768, I=384, E_global=16, E_local=16, topk=4, dtype="mxfp8", layout="compact", drop_every=7),
     dict(T=150, K=512, I=256, E_global=64, E_local=8, topk=8, dtype="mxfp8", layout="masked", expert_start=8),
+    dict(T=333, K=768, I=384, E_global=16, E_local=16, topk=4, dtype="mxfp4", layout="compact", drop_every=7),
+    dict(T=150, K=512, I=256, E_global=64, E_local=8, topk=8, dtype="mxfp4", layout="masked", expert_start=8),
 ]
 
 
@@ -52,7 +54,7 @@ def test_forward_matches_oracle(case):
 
 
 @pytest.mark.parametrize("T", [97, 40])   # 40: one partial block per masked expert
-@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "mxfp4", "bf16"])
 def test_masked_and_compact_agree_bitwise(dtype, T):
     kw = dict(T=T, K=512, I=256, E_global=32, E_local=32, topk=4, dtype=dtype, seed=11)
     pc = Problem(**kw, layout="compact")
@@ -137,10 +139,20 @@ def test_mxfp8_zipf_prefill_full_size_sampled():
     assert np.isfinite(out).all()
 
 
-@pytest.mark.parametrize("T", [1, 64])
-def test_mxfp8_masked_decode_full_size_sampled(T):
+def test_mxfp4_zipf_prefill_full_size_sampled():
     w = synth.WORKLOADS["fp8_prefill_zipf"]
-    p = Problem(T=T, K=w["K"], I=w["I"], E_global=256, E_local=32, topk=8, dtype="mxfp8", layout="masked",
+    p = Problem(T=w["T"], K=w["K"], I=w["I"], E_global=w["E_global"], E_local=w["E_local"], topk=w["topk"],
+                dtype="mxfp4", layout="compact", seed=w["seed"], zipf_s=w["zipf_s"])
+    g = p.gpu()
+    out = _sampled_check(p, g, [0, 8191])
+    assert np.isfinite(out).all()
+
+
+@pytest.mark.parametrize("dtype", ["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("T", [1, 64])
+def test_mx_masked_decode_full_size_sampled(T, dtype):
+    w = synth.WORKLOADS["fp8_prefill_zipf"]
+    p = Problem(T=T, K=w["K"], I=w["I"], E_global=256, E_local=32, topk=8, dtype=dtype, layout="masked",
                 max_m=(T + 15) // 16 * 16, seed=w["seed"] + T, weight_seed=w["seed"] + 2)
     g = p.gpu()
     _sampled_check(p, g, sorted({0, T - 1}))

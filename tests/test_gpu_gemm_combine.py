@@ -31,6 +31,9 @@ CASES = [
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
     dict(T=128, K=256, I=256, E_global=8, E_local=8, topk=2, dtype="mxfp8", layout="compact"),
+    dict(T=128, K=256, I=256, E_global=8, E_local=8, topk=2, dtype="mxfp4", layout="compact"),
+    dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="mxfp4", layout="compact", drop_every=5),
+    dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp4", layout="masked", expert_start=16),
     dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="mxfp8", layout="compact", drop_every=5),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
 ]
@@ -71,7 +74,7 @@ def test_gemm1_act_matches_oracle(case):
         h_ref[sel], _ = oracle.store_act(h, p.dtype)
     err = rel_fro(h_gpu, h_ref)
     assert err <= 2e-3, err
-    if p.dtype in ("fp8", "mxfp8"):
+    if p.dtype in ("fp8", "mxfp8", "mxfp4"):
         flips = np.mean(h_gpu != h_ref)
         assert flips <= 5e-3, flips
 

@@ -38,6 +38,13 @@ def weights_mx():
 
 
 @pytest.fixture(scope="module")
+def weights_mx4():
+    w13, w13s = synth.mxfp4_expert_weights(E, 2 * I, K, SEED + 2, "cuda")
+    w2, w2s = synth.mxfp4_expert_weights(E, K, I, SEED + 3, "cuda")
+    return w13, M.moe_pack_mx_scales(w13s), w2, M.moe_pack_mx_scales(w2s)
+
+
+@pytest.fixture(scope="module")
 def weights_bf16():
     return synth.bf16_expert_weights(E, 2 * I, K, SEED + 2, "cuda"), synth.bf16_expert_weights(E, K, I, SEED + 3, "cuda")
 
@@ -45,7 +52,7 @@ def weights_bf16():
 def _run(dtype, weights, x, ids, w):
     T = x.shape[0]
     shape = M.make_shape(T, K, I, E, E, TOPK, dtype, "compact")
-    if dtype in ("fp8", "mxfp8"):
+    if dtype in ("fp8", "mxfp8", "mxfp4"):
         ctx = M.moe_ctx_create(shape, weights[0], weights[1], weights[2], weights[3])
     else:
         ctx = M.moe_ctx_create(shape, weights[0], None, weights[1], None)
@@ -57,9 +64,10 @@ def _run(dtype, weights, x, ids, w):
     return out
 
 
-@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "mxfp4", "bf16"])
 def test_batch_invariance_sweep(dtype, request):
-    weights = request.getfixturevalue({"fp8": "weights_fp8", "mxfp8": "weights_mx", "bf16": "weights_bf16"}[dtype])
+    weights = request.getfixturevalue({"fp8": "weights_fp8", "mxfp8": "weights_mx", "mxfp4": "weights_mx4",
+                                       "bf16": "weights_bf16"}[dtype])
     n_probe = 4
     px, pids, pw = synth.probe_tokens(n_probe, K, E, TOPK, SEED, zipf_s=1.2)
     ref = None

@@ -23,6 +23,7 @@ CASES = [
     dict(T=0, K=256, I=128, E_global=8, E_local=8, topk=2, dtype="fp8", layout="compact"),
     dict(T=300, K=2304, I=128, E_global=16, E_local=16, topk=4, dtype="mxfp8", layout="compact", drop_every=5),
     dict(T=77, K=384, I=128, E_global=64, E_local=32, topk=8, dtype="mxfp8", layout="masked", expert_start=32),
+    dict(T=65, K=512, I=128, E_global=16, E_local=16, topk=4, dtype="mxfp4", layout="compact"),
 ]
 
 
@@ -81,7 +82,7 @@ def test_quant_scatter_matches_oracle_bit_exact(case):
     a = g.view("a")
     got = a.index_select(0, torch.as_tensor(rows, device=a.device)).cpu()
     x64 = p.x64()
-    if p.dtype in ("fp8", "mxfp8"):
+    if p.dtype in ("fp8", "mxfp8", "mxfp4"):   # MXFP4 weights keep MXFP8 activations
         q, s = oracle.quant_fp8_1x128(x64) if p.dtype == "fp8" else oracle.quant_mxfp8_1x32(x64)
         assert np.array_equal(got.numpy(), oracle.e4m3_bits(q)[toks])
         assert np.array_equal(g.sf_bytes("a_sf", rows), (s + 127).astype(np.uint8)[toks])
