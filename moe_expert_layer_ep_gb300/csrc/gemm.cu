@@ -57,15 +57,18 @@ namespace {
 // accumulator out and releases it before the activation and quantisation.
 // The others use 4 warps that interleave tensor-memory loads and stores
 // chunk by chunk (measured faster there).
-// MXFP4 weights: GEMM1 keeps 4 epilogue warps (each 32-column chunk is one
-// 1x32 scale group, so no amax exchange is needed) and the registers go to
-// 4 warps that expand the FP4 weights to e4m3 in shared memory.
-__host__ __device__ constexpr int epi_warps(bool fp8, int stage, bool fp4 = false) {
-  return (fp8 && stage == 1 && !fp4) ? 8 : 4;
+// MXFP4 weights add warps that expand the FP4 weights to e4m3 in shared
+// memory.  kFP4 = 1 (compact layouts, throughput): 4 epilogue warps (each
+// 32-column chunk of GEMM1 is one MXFP8 group of h) and 4 converter warps.
+// kFP4 = 2 (masked layouts, decode; GEMM1 only): the 8-warp early-release
+// epilogue and 2 converter warps (the register file allows no more).  Both
+// compute h with the same per-element operations, so they agree bitwise.
+__host__ __device__ constexpr int epi_warps(bool fp8, int stage, int fp4 = 0) {
+  return (fp8 && stage == 1 && fp4 != 1) ? 8 : 4;
 }
-constexpr int kConvWarps = 4;
-__host__ __device__ constexpr int threads_for(bool fp8, int stage, bool fp4) {
-  return 64 + 32 * epi_warps(fp8, stage, fp4) + (fp4 ? 32 * kConvWarps : 0);
+__host__ __device__ constexpr int conv_warps(int stage, int fp4) { return fp4 == 0 ? 0 : (stage == 1 && fp4 == 2 ? 2 : 4); }
+__host__ __device__ constexpr int threads_for(bool fp8, int stage, int fp4) {
+  return 64 + 32 * epi_warps(fp8, stage, fp4) + 32 * conv_warps(stage, fp4);
 }
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
@@ -78,18 +81,18 @@ constexpr int kSfbBytes = 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;               // FP8: scale tiles live in columns 256..383
 
-// Shared-memory map.  MXFP4 weights add a packed B buffer per stage, so 3
-// stages fit instead of 4.
+// Shared-memory map.  MXFP4 weights land packed in the upper half of the
+// stage's own B region and are expanded in place, so the FP4 pipeline keeps
+// the 4 stages of 48 KB.
 template <bool kFP4>
 struct Lay {
-  static constexpr int kStages = kFP4 ? 3 : 4;
+  static constexpr int kStages = 4;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
-  static constexpr int kOffBP = kOffB + kStages * kBBytes;
-  static constexpr int kOffSfa = kOffBP + (kFP4 ? kStages * kBPBytes : 0);
+  static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4;   // full, empty, conv; acc; done; amax exchange
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4 + 1;   // full, empty, conv; acc; done; amax; csync
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
@@ -159,13 +162,13 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
 
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
-template <bool kFP8, bool kMX, int kStage, bool kFP4>
+template <bool kFP8, bool kMX, int kStage, int kFP4>
 __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const GemmArgs g) {
-  using L = Lay<kFP4>;
+  using L = Lay<(kFP4 != 0)>;
   constexpr int kStages = L::kStages;
-  constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffBP = L::kOffBP, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
+  constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
   constexpr int kOffBar = L::kOffBar, kOffHolder = L::kOffHolder, kOffAbort = L::kOffAbort, kOffAmax = L::kOffAmax;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -178,6 +181,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
   uint64_t* done = bars + 2 * kStages + 4;
   uint64_t* xchg = bars + 2 * kStages + 5;  // [4]: the two epilogue warps of a lane quadrant
   uint64_t* conv = bars + 2 * kStages + 9;  // [kStages] MXFP4: B expanded to e4m3
+  uint64_t* csync = bars + 3 * kStages + 9; // MXFP4: all converter threads have read the packed tile
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kOffHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
@@ -194,8 +198,10 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     }
     mbar_init(done, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&xchg[q], 64);
-    if (kFP4)
-      for (int s = 0; s < kStages; ++s) mbar_init(&conv[s], 32 * kConvWarps);
+    if (kFP4) {
+      for (int s = 0; s < kStages; ++s) mbar_init(&conv[s], 32 * conv_warps(kStage, kFP4));
+      mbar_init(csync, 32 * conv_warps(kStage, kFP4));
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
@@ -265,10 +271,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
           const int kc = kb * kElemsPerKBlock;
           tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
           if (kFP4) {
-            // packed E2M1 rows, 64 bytes per row per K block, unswizzled
-            tma_load_3d(smem + kOffBP + stage * kBPBytes, &map_b, &full[stage], kc / 2, r0, tl.expert);
-            tma_load_3d(smem + kOffBP + stage * kBPBytes + kBPBytes / 2, &map_b, &full[stage], kc / 2, r1,
-                        tl.expert);
+            // packed E2M1 rows, 64 bytes per row per K block, unswizzled, into
+            // the upper half of the stage's B region (expanded in place)
+            uint8_t* bp = smem + kOffB + stage * kBBytes + kBBytes / 2;
+            tma_load_3d(bp, &map_b, &full[stage], kc / 2, r0, tl.expert);
+            tma_load_3d(bp + kBPBytes / 2, &map_b, &full[stage], kc / 2, r1, tl.expert);
           } else {
             tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, &full[stage], kc, r0, tl.expert);
             tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, &full[stage], kc, r1, tl.expert);
@@ -375,12 +382,17 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     }
   } else if (kFP4 && warp >= 2 + epi_warps(kFP8, kStage, kFP4)) {
     // ------------------------------------------------------------------ FP4 -> e4m3
-    // Each stage's packed B tile (256 rows x 64 bytes) becomes the e4m3 B
-    // tile (two 128-row boxes of 128-byte rows, 128-byte swizzle: 16-byte
-    // chunk c of row r at r * 128 + ((c ^ (r % 8)) * 16)).
+    // Each stage's packed B tile (256 rows x 64 bytes, in the upper half of
+    // the B region) becomes the e4m3 B tile over the whole region (two
+    // 128-row boxes of 128-byte rows, 128-byte swizzle: 16-byte chunk c of row
+    // r at r * 128 + ((c ^ (r % 8)) * 16)).  The output overwrites packed
+    // bytes, so every converter thread first reads its share into registers
+    // and the converter warps meet on an mbarrier before anyone writes.
+    constexpr int kConv = conv_warps(kStage, kFP4) > 0 ? conv_warps(kStage, kFP4) : 1;   // (not FP4: unused)
+    constexpr int kChunks = kTileN * 8 / (32 * kConv);   // 16-byte output chunks per thread
     const int ct = threadIdx.x - 32 * (2 + epi_warps(kFP8, kStage, kFP4));
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, sync_phase = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       for (int kb = 0; kb < k_blocks; ++kb) {
@@ -389,15 +401,28 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
           ok = false;
           break;
         }
-        const uint8_t* src = smem + kOffBP + stage * kBPBytes;
         uint8_t* dst = smem + kOffB + stage * kBBytes;
-#pragma unroll 4
-        for (int q = ct; q < kTileN * 8; q += 32 * kConvWarps) {
+        const uint8_t* src = dst + kBBytes / 2;
+        uint2 pk[kChunks];
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int q = ct + i * 32 * kConv;
+          pk[i] = *reinterpret_cast<const uint2*>(src + (q >> 3) * 64 + (q & 7) * 8);
+        }
+        mbar_arrive(csync);
+        const bool met = mbar_wait_bounded(csync, sync_phase, abort_flag, g.timeout_ns);
+        sync_phase ^= 1;
+        if (!__all_sync(0xFFFFFFFFu, met)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int q = ct + i * 32 * kConv;
           const int row = q >> 3, c = q & 7;
-          const uint2 pk = *reinterpret_cast<const uint2*>(src + row * 64 + c * 8);
           uint4 o;
-          fp4x8_to_e4m3(pk.x, &o.x, &o.y);
-          fp4x8_to_e4m3(pk.y, &o.z, &o.w);
+          fp4x8_to_e4m3(pk[i].x, &o.x, &o.y);
+          fp4x8_to_e4m3(pk[i].y, &o.z, &o.w);
           *reinterpret_cast<uint4*>(dst + (row >> 7) * (kBBytes / 2) + (row & 127) * 128 + ((c ^ (row & 7)) << 4)) = o;
         }
         fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor cores
@@ -639,9 +664,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
   }
 }
 
-template <bool kFP8, bool kMX, int kStage, bool kFP4 = false>
+template <bool kFP8, bool kMX, int kStage, int kFP4 = 0>
 cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
-  constexpr int kSmemBytes = Lay<kFP4>::kSmemBytes;
+  constexpr int kSmemBytes = Lay<(kFP4 != 0)>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>,
@@ -674,8 +699,8 @@ int gemm_smem_bytes(int fp4) { return fp4 ? Lay<true>::kSmemBytes : Lay<false>::
 
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
   if (g.fp4) {
-    return g.stage == 1 ? launch_one<true, true, 1, true>(g, a, b, grid, s)
-                        : launch_one<true, true, 2, true>(g, a, b, grid, s);
+    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, a, b, grid, s);
+    return g.masked ? launch_one<true, true, 1, 2>(g, a, b, grid, s) : launch_one<true, true, 1, 1>(g, a, b, grid, s);
   }
   if (g.mx) {
     return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, grid, s) : launch_one<true, true, 2>(g, a, b, grid, s);
