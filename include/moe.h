@@ -8,11 +8,15 @@
  *        (sglang PR #38160 report)
  *
  *   plan_layout      top-k routing -> per-expert row layout      [P1 "实现拆解" 2-3]
- *   quant_scatter    x -> FP8 1x128 UE8M0 (or BF16) expert rows   [P1 "实现拆解" 3, P2 step 3]
+ *   quant_scatter    x -> FP8 1x128 / MXFP8 1x32 UE8M0 (or BF16) expert rows
+ *                                                                [P1 "实现拆解" 3, "风险与影响" 5; P2 step 3]
  *   grouped_gemm_w13_act   h = silu(a W1^T) * (a W3^T)            [P2 "关键源码片段" deep_gemm.py]
  *   grouped_gemm_w2        y = h W2^T                             [P2 same]
  *   combine          out[t] = sum_j w[t,j] * y[src2dst[t,j]]      [P1 "风险与影响" 2, P3 "实现拆解" 3]
  *   forward          all five, in order, on one stream
+ * and, around the layer: load-time weight preparation (UE8M0 requantisation,
+ * MXFP8 / MXFP4 scale packing) and the fp32 router that produces the routing
+ * input.
  *
  * Conventions for every call below
  * --------------------------------

@@ -27,15 +27,19 @@
 // its 1x128 UE8M0 quantisation without leaving the CTA.  Stage 2's B tile is
 // 256 consecutive rows of w2.
 //
-// One persistent CTA per SM, 10 warps:
+// The MXFP4 variant (FP4 E2M1 weights with 1x32 scales, the FP4 item of
+// the same list) loads the packed weights into the upper half of each
+// stage's B region and expands them in place to e4m3 (exact) before the same
+// MMA runs.
+//
+// One persistent CTA per SM:
 //   warp 0      TMA producer (A tile, B tiles, activation scale chunk; weight
-//               scales expanded into shared memory)
+//               scales expanded into shared memory, or bulk-copied for MX)
 //   warp 1      TMEM allocation + single-thread MMA issue (tcgen05.cp of the
 //               scale tiles, 4 MMAs of K=32 bytes per 128-byte K block)
-//   warps 2-9   epilogue, two warps per accumulator lane quadrant (warp % 4),
-//               each with half of the columns: tcgen05.ld, release of the
-//               accumulator, then activation / quantisation and stores of
-//               valid rows
+//   epilogue    4 or 8 warps (see epi_warps): tcgen05.ld of the accumulator,
+//               then activation / quantisation and stores of valid rows
+//   converters  MXFP4 only, 2 or 4 warps (see conv_warps): FP4 -> e4m3
 // A 4-stage mbarrier ring connects producer and MMA; accumulator barriers
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
 // path, whose other tensor-memory columns hold the scale tiles).
@@ -695,7 +699,6 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 
 }  // namespace
 
-int gemm_smem_bytes(int fp4) { return fp4 ? Lay<true>::kSmemBytes : Lay<false>::kSmemBytes; }
 
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
   if (g.fp4) {

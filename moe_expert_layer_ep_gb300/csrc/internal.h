@@ -109,7 +109,5 @@ cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, con
                          float* logits, int32_t* ids, float* wts, cudaStream_t s);
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s);
 
-int plan_launches();
-int gemm_smem_bytes(int fp8);
 
 }  // namespace moe
