@@ -120,20 +120,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def kernel_source_digest():
+    """Digest of the GEMM kernel sources with // comments and blank lines
+    removed, so that a comment-only edit keeps a capture valid."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "moe_expert_layer_ep_gb300", "csrc")
+    parts = []
+    for f in ("gemm.cu", "common.cuh"):
+        code = re.sub(r"//[^\n]*", "", open(os.path.join(csrc, f)).read())
+        code = "\n".join(l.rstrip() for l in code.splitlines() if l.strip())
+        parts.append(hashlib.sha256(code.encode()).hexdigest()[:16])
+    return "-".join(parts)
+
+
 def measured_traffic(workload_name):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel sources changed since the capture."""
-    import hashlib
+    summary, or None when the kernel code changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path)).get(workload_name)
     if not rec:
         return None
-    csrc = os.path.join(ROOT, "moe_expert_layer_ep_gb300", "csrc")
-    sha = "-".join(hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()[:16]
-                   for f in ("gemm.cu", "common.cuh"))
-    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256_16"] else None
+    return rec["dram_bytes_per_launch"] if kernel_source_digest() == rec["code_digest"] else None
 
 
 def workload(args):
