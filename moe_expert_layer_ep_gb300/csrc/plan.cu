@@ -91,6 +91,58 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return warp_base + x - v;
 }
 
+// From the per-expert counts (s_count, shared): padded sizes, expert starts,
+// masked row counts, the 128-row block table and meta.  Called by all 1024
+// threads of the block (thread e handles local expert e).  When s_start is
+// given, each expert's first row is also left there.
+__device__ void expert_tables(const PlanArgs& p, const int* s_count, int* s_warp, int* s_start) {
+  const int e = threadIdx.x;
+  const bool act = e < p.E_local;
+  const int count = act ? s_count[e] : 0;
+  int rows, nblk;
+  if (!p.masked) {
+    rows = (count + kBlockM - 1) / kBlockM * kBlockM;
+    nblk = rows / kBlockM;
+  } else {
+    if (count > p.max_m) set_status(p.status, MOE_ERR_MASKED_OVERFLOW);
+    rows = count < p.max_m ? count : static_cast<int>(p.max_m);
+    nblk = (rows + kBlockM - 1) / kBlockM;
+  }
+  int total_rows, total_blk;
+  const int row_start = block_exclusive_scan(act ? rows : 0, s_warp, &total_rows);
+  const int blk_start = block_exclusive_scan(act ? nblk : 0, s_warp, &total_blk);
+  if (act) {
+    if (s_start) s_start[e] = row_start;
+    p.counts[e] = count;
+    if (!p.masked) {
+      p.padded[e] = rows;
+      p.start[e] = row_start;
+    } else {
+      p.masked_m[e] = rows;
+    }
+    for (int b = 0; b < nblk; ++b) {
+      int4 info;
+      info.x = e;
+      if (!p.masked) {
+        info.y = row_start + b * kBlockM;
+        info.z = info.y;
+        const int left = count - b * kBlockM;
+        info.w = left < kBlockM ? left : kBlockM;
+      } else {
+        info.y = static_cast<int>(static_cast<int64_t>(e) * p.max_m + b * kBlockM);
+        info.z = b * kBlockM;
+        const int left = rows - b * kBlockM;
+        info.w = left < kBlockM ? left : kBlockM;
+      }
+      reinterpret_cast<int4*>(p.block_info)[blk_start + b] = info;
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.meta[0] = total_rows;
+    p.meta[1] = total_blk;
+  }
+}
+
 __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
   __shared__ int s_warp[32];
   __shared__ int s_count[kMaxLocalExperts];
@@ -126,49 +178,33 @@ __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
     if (lane == 0) s_count[ex] = carry;
   }
   __syncthreads();
-  const int e = threadIdx.x;
-  const bool act = e < p.E_local;
-  const int count = act ? s_count[e] : 0;
-  int rows, nblk;
-  if (!p.masked) {
-    rows = (count + kBlockM - 1) / kBlockM * kBlockM;
-    nblk = rows / kBlockM;
-  } else {
-    if (count > p.max_m) set_status(p.status, MOE_ERR_MASKED_OVERFLOW);
-    rows = count < p.max_m ? count : static_cast<int>(p.max_m);
-    nblk = (rows + kBlockM - 1) / kBlockM;
-  }
-  int total_rows, total_blk;
-  const int row_start = block_exclusive_scan(act ? rows : 0, s_warp, &total_rows);
-  const int blk_start = block_exclusive_scan(act ? nblk : 0, s_warp, &total_blk);
-  if (act) {
-    p.counts[e] = count;
-    if (!p.masked) {
-      p.padded[e] = rows;
-      p.start[e] = row_start;
-    } else {
-      p.masked_m[e] = rows;
-    }
-    for (int b = 0; b < nblk; ++b) {
-      int4 info;
-      info.x = e;
-      if (!p.masked) {
-        info.y = row_start + b * kBlockM;
-        info.z = info.y;
-        const int left = count - b * kBlockM;
-        info.w = left < kBlockM ? left : kBlockM;
+  expert_tables(p, s_count, s_warp, nullptr);
+}
+
+// m_indices[r] for rows r = first, first + stride, ...: the local expert
+// whose padded segment holds row r if r is one of its first counts[e] rows,
+// else -1.  s_tab: start[E], padded[E], counts[E].
+__device__ void fill_m_indices(const PlanArgs& p, const int32_t* s_tab, int64_t first, int64_t stride) {
+  const int E = p.E_local;
+  for (int64_t r = first; r < p.all_tokens; r += stride) {
+    // last expert whose start is <= r (empty experts share starts; the last
+    // one with that start owns the rows)
+    int lo = 0, hi = E - 1, found = -1;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_tab[mid] <= r) {
+        found = mid;
+        lo = mid + 1;
       } else {
-        info.y = static_cast<int>(static_cast<int64_t>(e) * p.max_m + b * kBlockM);
-        info.z = b * kBlockM;
-        const int left = rows - b * kBlockM;
-        info.w = left < kBlockM ? left : kBlockM;
+        hi = mid - 1;
       }
-      reinterpret_cast<int4*>(p.block_info)[blk_start + b] = info;
     }
-  }
-  if (threadIdx.x == 0) {
-    p.meta[0] = total_rows;
-    p.meta[1] = total_blk;
+    int32_t v = -1;
+    if (found >= 0) {
+      const int64_t off = r - s_tab[found];
+      if (off < s_tab[E + found] && off < s_tab[2 * E + found]) v = found;
+    }
+    p.m_indices[r] = v;
   }
 }
 
@@ -198,37 +234,89 @@ __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
     }
     p.src2dst[i] = dst;
   }
-  if (!p.masked) {
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < p.all_tokens; r += stride) {
-      // last expert whose start is <= r (empty experts share starts; the
-      // last one with that start owns the rows)
-      int lo = 0, hi = E - 1, found = -1;
-      while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_tab[mid] <= r) {
-          found = mid;
-          lo = mid + 1;
-        } else {
-          hi = mid - 1;
-        }
-      }
-      int32_t v = -1;
-      if (found >= 0) {
-        const int64_t off = r - s_tab[found];
-        if (off < s_tab[E + found] && off < s_tab[2 * E + found]) v = found;
-      }
-      p.m_indices[r] = v;
+  if (!p.masked)
+    fill_m_indices(p, s_tab, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x, stride);
+}
+
+// Small problems (decode): the whole plan in one CTA.  Assignments are
+// taken in 1024-wide chunks in flattened order; an assignment's stable rank
+// is the expert's count in earlier chunks + in earlier warps of its chunk +
+// in earlier lanes of its warp (warp match), as in the three-kernel path, so
+// the outputs are identical to it.
+constexpr int kPlanSmallMaxA = 2048;
+constexpr int kPlanSmallMaxE = 256;
+
+__global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
+  __shared__ int s_wcnt[32 * kPlanSmallMaxE];   // [warp][expert] counts of the current chunk
+  __shared__ int s_tab[3 * kPlanSmallMaxE];     // start, padded, counts (the running per-expert counts)
+  __shared__ int s_warp[32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E_local;
+  int* s_count = s_tab + 2 * E;
+  for (int x = tid; x < E; x += 1024) s_count[x] = 0;
+  int my_e[2] = {-1, -1};
+  int rank[2] = {0, 0};
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = tid + 1024 * k;
+    for (int x = tid; x < 32 * E; x += 1024) s_wcnt[x] = 0;
+    int e = -1;
+    if (i < p.A) {
+      bool bad;
+      e = local_expert(p.topk_ids[i], p.E_global, p.E_local, p.expert_start, &bad);
+      if (bad) set_status(p.status, MOE_ERR_EXPERT_ID);
     }
+    my_e[k] = e;
+    __syncthreads();
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const unsigned lower = peers & ((1u << lane) - 1u);
+    if (e >= 0 && lower == 0) s_wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int prefix = s_count[e];
+      for (int w = 0; w < warp; ++w) prefix += s_wcnt[w * E + e];
+      rank[k] = prefix + __popc(lower);
+    }
+    __syncthreads();
+    for (int x = tid; x < E; x += 1024) {
+      int add = 0;
+      for (int w = 0; w < 32; ++w) add += s_wcnt[w * E + x];
+      s_count[x] += add;
+    }
+    __syncthreads();
   }
+  expert_tables(p, s_count, s_warp, s_tab);
+  if (!p.masked)
+    for (int x = tid; x < E; x += 1024) s_tab[E + x] = p.padded[x];
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = tid + 1024 * k;
+    if (i >= p.A) continue;
+    const int e = my_e[k];
+    int32_t dst = -1;
+    if (e >= 0) {
+      if (!p.masked) {
+        dst = s_tab[e] + rank[k];
+      } else if (rank[k] < p.max_m) {
+        dst = static_cast<int32_t>(static_cast<int64_t>(e) * p.max_m + rank[k]);
+      }
+    }
+    p.src2dst[i] = dst;
+  }
+  if (!p.masked) fill_m_indices(p, s_tab, tid, 1024);
 }
 
 }  // namespace
-
 
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s) {
   // the status word reports the first data error of this pass through the layer
   cudaError_t e = cudaMemsetAsync(p.status, 0, 16, s);
   if (e != cudaSuccess) return e;
+  if (p.A <= kPlanSmallMaxA && p.E_local <= kPlanSmallMaxE) {
+    plan_small<<<1, 1024, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   if (p.chunks > 0) {
     plan_count_rank<<<p.chunks, kPlanChunk, 8 * p.E_local * sizeof(int32_t), s>>>(p);
   }
