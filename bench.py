@@ -56,6 +56,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms, world, device):
+    """The slowest rank's time: every replica's batch counts toward `value`,
+    so the job takes as long as its slowest rank."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(tokens_per_rank, world, steps, ms):
+    """Whole-job throughput: the tokens all ranks processed / the max time."""
+    return world * tokens_per_rank * steps / (ms / 1000.0)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -345,10 +360,7 @@ def run_ours(args, w, world, rank, local):
     total_ms = t0.elapsed_time(t1)
     stage_ms = np.array([[ev[s][i].elapsed_time(ev[s][i + 1]) for i in range(nst)]
                          for s in range(args.steps)])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # end to end through the C-ABI with host buffers, as a serving loop runs
     # it: every step copies its x / ids / weights from pinned host memory and
@@ -404,10 +416,7 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.synchronize()
     assert torch.equal(out_h[(args.steps - 1) & 1].view(torch.int16), out.cpu().view(torch.int16))
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     assert M.moe_read_device_status(ws) == 0
 
     if rank != 0:
@@ -416,7 +425,7 @@ def run_ours(args, w, world, rank, local):
     wm = work_model(w, ids_host)
     T = w["T"]
     ms_per_step = total_ms / args.steps
-    value = world * T * args.steps / (total_ms / 1000.0)
+    value = replica_value(T, world, args.steps, total_ms)
     med = np.median(stage_ms, axis=0)
     g1_ms, g2_ms = float(med[2]), float(med[3])
     gemm_tflops = (wm["flops1"] + wm["flops2"]) / ((g1_ms + g2_ms) / 1000.0) / 1e12
@@ -454,7 +463,7 @@ def run_ours(args, w, world, rank, local):
                                                             "combine"], med)},
         "roofline": roof,
         "clocks": clk.summary(),
-        "e2e": {"value": round(world * T * args.steps / (e2e_ms / 1000.0), 1), "unit": "tokens/s",
+        "e2e": {"value": round(replica_value(T, world, args.steps, e2e_ms), 1), "unit": "tokens/s",
                 "pipelining": "h2d / d2h on copy streams overlapping the neighbouring steps' forwards",
                 "h2d_bytes_per_step": x.numel() * 2 + ids.numel() * 4 + wts.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
