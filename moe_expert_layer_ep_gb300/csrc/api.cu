@@ -391,7 +391,7 @@ moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_i
 int32_t moe_forward_launches(const moe_ctx* ctx) {
   if (!ctx) return -1;
   const moe_shape_t& s = ctx->shape;
-  int n = (ctx->ws.chunks > 0 ? 1 : 0) + 2;  // plan
+  int n = moe::plan_launch_count(s.T * s.topk, s.E_local);   // plan
   if (s.T > 0) n += 2;                          // quant + combine
   if (ctx->ws.blocks > 0) n += 2;               // two GEMMs
   return n;

@@ -86,6 +86,7 @@ struct GemmArgs {
 };
 
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
+int plan_launch_count(int64_t A, int32_t E_local);   // kernels one launch_plan enqueues
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
 cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUtensorMap& map_b, int grid,

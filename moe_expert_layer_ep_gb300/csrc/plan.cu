@@ -309,11 +309,18 @@ __global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
 
 }  // namespace
 
+bool plan_is_small(int64_t A, int32_t E_local) { return A <= kPlanSmallMaxA && E_local <= kPlanSmallMaxE; }
+
+int plan_launch_count(int64_t A, int32_t E_local) {
+  if (plan_is_small(A, E_local)) return 1;
+  return (A > 0 ? 1 : 0) + 2;   // count_rank (when there are assignments), scan, finalize
+}
+
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s) {
   // the status word reports the first data error of this pass through the layer
   cudaError_t e = cudaMemsetAsync(p.status, 0, 16, s);
   if (e != cudaSuccess) return e;
-  if (p.A <= kPlanSmallMaxA && p.E_local <= kPlanSmallMaxE) {
+  if (plan_is_small(p.A, p.E_local)) {
     plan_small<<<1, 1024, 0, s>>>(p);
     return cudaGetLastError();
   }
