@@ -156,3 +156,24 @@ def test_mx_masked_decode_full_size_sampled(T, dtype):
                 max_m=(T + 15) // 16 * 16, seed=w["seed"] + T, weight_seed=w["seed"] + 2)
     g = p.gpu()
     _sampled_check(p, g, sorted({0, T - 1}))
+
+
+@pytest.mark.parametrize("case", [dict(T=40, layout="masked", E_global=64, E_local=8),
+                                  dict(T=600, layout="compact", E_global=16, E_local=16)])
+def test_forward_launch_count_matches_profiler(case):
+    """moe_forward_launches (what the bench reports as gpu_launches) equals the
+    libmoe kernels a profiler sees in one forward (small and large plans)."""
+    import moe_expert_layer_ep_gb300 as M
+    profiler = pytest.importorskip("torch.profiler")
+    p = Problem(K=256, I=128, topk=8, dtype="fp8", **case)
+    g = p.gpu()
+    g.forward()
+    torch.cuda.synchronize()
+    with profiler.profile(activities=[profiler.ProfilerActivity.CUDA]) as prof:
+        g.forward()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events()]
+    if not names:
+        pytest.skip("the profiler records no device activity in this environment")
+    ours = [n for n in names if any(k in n for k in ("plan_", "quant_scatter", "grouped_gemm", "combine_kernel"))]
+    assert len(ours) == M.moe_forward_launches(g.ctx), (ours, len(names), names[:20])
