@@ -475,7 +475,7 @@ def run_ours(args, w, world, rank, local):
         "work": {"assignments": wm["A"], "nonempty_experts": wm["nonempty"],
                  "padded_rows": int(M.ws_view(ctx, ws, "meta")[0].item())},
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:       # timed beside the N=1 line only
         cb = OracleRunner(w, x, ids_host, w_host, weights).run(seconds_target=12.0)
         cb.pop("tokens")
         line["cpu_baseline"] = cb
