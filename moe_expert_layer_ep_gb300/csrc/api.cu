@@ -31,6 +31,7 @@ struct moe_ctx {
   const void* ws_for_maps;
   CUtensorMap map_a;
   CUtensorMap map_h;
+  CUtensorMap map_y;   // GEMM2 output, 32-column store boxes
   uint64_t timeout_ns;
 };
 
@@ -61,18 +62,19 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 // 128 rows, 128-byte swizzle (the layout the MMA descriptors expect).
 // packed4: byte rows of packed FP4 codes, a 64-byte inner box, no swizzle
 // (the kernel expands them into the swizzled e4m3 layout itself).
+// store64: a 64-byte inner box with 64-byte swizzle (the GEMM2 output stores).
 moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-                      bool packed4 = false) {
+                      bool packed4 = false, bool store64 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
   const uint64_t esize = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
   cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>((packed4 ? 64 : 128) / esize), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>((packed4 || store64 ? 64 : 128) / esize), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  packed4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  packed4 ? CU_TENSOR_MAP_SWIZZLE_NONE : (store64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B),
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -161,6 +163,8 @@ moe_status_t ensure_ws_maps(moe_ctx* c, void* ws) {
     moe_status_t st = make_map(&c->map_a, at<uint8_t>(ws, c->ws.a), c->fp8, s.K, d1, d2);
     if (st != MOE_OK) return st;
     st = make_map(&c->map_h, at<uint8_t>(ws, c->ws.h), c->fp8, s.I, d1, d2);
+    if (st != MOE_OK) return st;
+    st = make_map(&c->map_y, at<uint8_t>(ws, c->ws.y), false, s.K, d1, d2, false, true);
     if (st != MOE_OK) return st;
   }
   c->ws_for_maps = ws;
@@ -354,7 +358,8 @@ static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
   if (max_tiles < grid) grid = static_cast<int>(max_tiles);
   const CUtensorMap& a = stage == 1 ? ctx->map_a : ctx->map_h;
   const CUtensorMap& b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
-  return cuda_status(moe::launch_gemm(g, a, b, grid, static_cast<cudaStream_t>(stream)));
+  const CUtensorMap& out = stage == 1 ? ctx->map_a : ctx->map_y;   // stage 1 stores through plain writes
+  return cuda_status(moe::launch_gemm(g, a, b, out, grid, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_grouped_gemm_w13_act(moe_ctx* ctx, void* ws, void* stream) { return run_gemm(ctx, ws, stream, 1); }

@@ -96,11 +96,14 @@ struct Lay {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4 + 1;   // full, empty, conv; acc; done; amax; csync
+  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4 + 1 + 1;   // full, empty, conv; acc; done; amax; csync; esync
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
-  static constexpr int kSmemBytes = kOffAmax + 2 * 4 * 2 * 32 * 4 + 1024;   // + 1024-byte alignment slack
+  // GEMM2 output staging for TMA stores: two 128-row x 32-column bf16 tiles
+  static constexpr int kOffStage = (kOffAmax + 2 * 4 * 2 * 32 * 4 + 1023) / 1024 * 1024;
+  static constexpr int kStageTileBytes = kTileM * 64;
+  static constexpr int kSmemBytes = kOffStage + 2 * kStageTileBytes + 1024;   // + 1024-byte alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -169,7 +172,7 @@ __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / 
 template <bool kFP8, bool kMX, int kStage, int kFP4>
 __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap map_out, const GemmArgs g) {
   using L = Lay<(kFP4 != 0)>;
   constexpr int kStages = L::kStages;
   constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
   uint64_t* xchg = bars + 2 * kStages + 5;  // [4]: the two epilogue warps of a lane quadrant
   uint64_t* conv = bars + 2 * kStages + 9;  // [kStages] MXFP4: B expanded to e4m3
   uint64_t* csync = bars + 3 * kStages + 9; // MXFP4: all converter threads have read the packed tile
+  uint64_t* esync = bars + 3 * kStages + 10; // GEMM2: the epilogue warps have staged a chunk
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kOffHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
@@ -206,6 +210,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
       for (int s = 0; s < kStages; ++s) mbar_init(&conv[s], 32 * conv_warps(kStage, kFP4));
       mbar_init(csync, 32 * conv_warps(kStage, kFP4));
     }
+    mbar_init(esync, 32 * epi_warps(kFP8, kStage, kFP4));
+    if (kStage == 2) prefetch_tensormap(&map_out);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
@@ -453,6 +459,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     const int r = quad * 32 + lane;
     float* s_amax = reinterpret_cast<float*>(smem + kOffAmax);  // [2 parities][4 quads][2 halves][32]
     int iter = 0;
+    uint32_t chunk_ctr = 0;   // GEMM2: staged chunks so far (staging tile and barrier parity)
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++iter) {
       const Tile tl = load_tile(g, t);
       const int acc = kFP8 ? 0 : (iter & 1);
@@ -632,8 +639,18 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
           }
         }
       } else {
+        // y: blocks with at least half of their rows valid go through shared
+        // memory and TMA stores (each 32-column chunk packed to bf16 into one
+        // of two staging tiles -- 64-byte rows, 64-byte swizzle: 16-byte piece
+        // j of row r at r * 64 + ((j ^ ((r >> 1) & 3)) * 16) -- then one
+        // thread stores the 128 x 32 tile; rows past the valid count land in
+        // the expert's padding (compact) or are clipped at max_m by the map
+        // (masked)).  Sparser blocks (decode) store their valid rows directly.
         const int64_t col0 = static_cast<int64_t>(tl.nb) * kTileN;
+        const bool use_tma = tl.valid >= kTileM / 2;     // uniform over the epilogue warps
+        const bool issuer = warp == 2 && lane == 0;
         uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + col0;
+        bool ok = true;
 #pragma unroll 1
         for (int c = 0; c < kTileN / 32; ++c) {
           uint32_t v32[32];
@@ -643,24 +660,53 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
             tc_fence_before();
             mbar_arrive(&tempty[acc]);
           }
-          if (row_ok && col0 + c * 32 < g.n_total) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          uint4 o[4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int b = v * 8;
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v32[b + 0]), __uint_as_float(v32[b + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v32[b + 2]), __uint_as_float(v32[b + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v32[b + 4]), __uint_as_float(v32[b + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v32[b + 6]), __uint_as_float(v32[b + 7]));
-              d4[v] = o;
-            }
+          for (int v = 0; v < 4; ++v) {
+            const int b = v * 8;
+            o[v].x = pack_bf16x2(__uint_as_float(v32[b + 0]), __uint_as_float(v32[b + 1]));
+            o[v].y = pack_bf16x2(__uint_as_float(v32[b + 2]), __uint_as_float(v32[b + 3]));
+            o[v].z = pack_bf16x2(__uint_as_float(v32[b + 4]), __uint_as_float(v32[b + 5]));
+            o[v].w = pack_bf16x2(__uint_as_float(v32[b + 6]), __uint_as_float(v32[b + 7]));
           }
+          if (!use_tma) {
+            if (row_ok && col0 + c * 32 < g.n_total) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) d4[v] = o[v];
+            }
+            continue;
+          }
+          uint8_t* stg = smem + L::kOffStage + (chunk_ctr & 1) * L::kStageTileBytes + r * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) *reinterpret_cast<uint4*>(stg + ((v ^ ((r >> 1) & 3)) << 4)) = o[v];
+          fence_proxy_async_smem();
+          // the previous chunk's store has read its staging tile, so the next
+          // chunk may overwrite it once everyone has passed this point
+          if (issuer) bulk_wait_read_all();
+          mbar_arrive(esync);
+          const bool met = mbar_wait_bounded(esync, chunk_ctr & 1, abort_flag, g.timeout_ns);
+          if (!__all_sync(0xFFFFFFFFu, met)) {
+            ok = false;
+            break;
+          }
+          if (issuer && col0 + c * 32 < g.n_total) {
+            tma_store_3d(&map_out, smem + L::kOffStage + (chunk_ctr & 1) * L::kStageTileBytes,
+                         static_cast<int32_t>(col0 + c * 32), tl.tma_row, g.masked ? tl.expert : 0);
+            bulk_commit_group();
+          }
+          ++chunk_ctr;
+        }
+        if (!ok) {
+          set_status(g.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          break;
         }
       }
     }
   }
 
+  if (kStage == 2 && warp == 2 && lane == 0) bulk_wait_all();   // the TMA stores of y have completed
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -669,7 +715,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
 }
 
 template <bool kFP8, bool kMX, int kStage, int kFP4 = 0>
-cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
+cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int grid,
+                       cudaStream_t s) {
   constexpr int kSmemBytes = Lay<(kFP4 != 0)>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
@@ -678,7 +725,7 @@ cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4><<<grid, threads_for(kFP8, kStage, kFP4), kSmemBytes, s>>>(a, b, g);
+  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4><<<grid, threads_for(kFP8, kStage, kFP4), kSmemBytes, s>>>(a, b, out, g);
   return cudaGetLastError();
 }
 
@@ -700,20 +747,21 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 }  // namespace
 
 
-cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int grid,
+                        cudaStream_t s) {
   if (g.fp4) {
-    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, a, b, grid, s);
-    return g.masked ? launch_one<true, true, 1, 2>(g, a, b, grid, s) : launch_one<true, true, 1, 1>(g, a, b, grid, s);
+    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, a, b, out, grid, s);
+    return g.masked ? launch_one<true, true, 1, 2>(g, a, b, out, grid, s) : launch_one<true, true, 1, 1>(g, a, b, out, grid, s);
   }
   if (g.mx) {
-    return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, grid, s) : launch_one<true, true, 2>(g, a, b, grid, s);
+    return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, out, grid, s) : launch_one<true, true, 2>(g, a, b, out, grid, s);
   }
   if (g.fp8) {
-    return g.stage == 1 ? launch_one<true, false, 1>(g, a, b, grid, s)
-                        : launch_one<true, false, 2>(g, a, b, grid, s);
+    return g.stage == 1 ? launch_one<true, false, 1>(g, a, b, out, grid, s)
+                        : launch_one<true, false, 2>(g, a, b, out, grid, s);
   }
-  return g.stage == 1 ? launch_one<false, false, 1>(g, a, b, grid, s)
-                      : launch_one<false, false, 2>(g, a, b, grid, s);
+  return g.stage == 1 ? launch_one<false, false, 1>(g, a, b, out, grid, s)
+                      : launch_one<false, false, 2>(g, a, b, out, grid, s);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {
