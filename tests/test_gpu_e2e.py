@@ -27,6 +27,7 @@ SMALL = [
     dict(T=150, K=512, I=256, E_global=64, E_local=8, topk=8, dtype="fp8", layout="masked", expert_start=8),
     dict(T=150, K=512, I=256, E_global=64, E_local=8, topk=8, dtype="bf16", layout="masked", expert_start=8),
     dict(T=600, K=512, I=256, E_global=8, E_local=8, topk=4, dtype="bf16", layout="compact", drop_every=7),
+    dict(T=600, K=512, I=256, E_global=8, E_local=8, topk=4, dtype="fp8", layout="compact", drop_every=7),
     dict(T=40, K=256, I=128, E_global=40, E_local=20, topk=3, dtype="fp8", layout="compact", expert_start=20),
     dict(T=333, K=768, I=384, E_global=16, E_local=16, topk=4, dtype="mxfp8", layout="compact", drop_every=7),
     dict(T=150, K=512, I=256, E_global=64, E_local=8, topk=8, dtype="mxfp8", layout="masked", expert_start=8),

@@ -25,9 +25,12 @@ CASES = [
     dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="bf16", layout="compact", drop_every=5),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
-    # BF16 with several 128-row blocks per expert, odd block counts included
+    # several 128-row blocks per expert, odd block counts included
     dict(T=700, K=384, I=256, E_global=8, E_local=8, topk=4, dtype="bf16", layout="compact", drop_every=5),
     dict(T=1100, K=256, I=256, E_global=16, E_local=4, topk=4, dtype="bf16", layout="masked", expert_start=4),
+    dict(T=700, K=384, I=256, E_global=8, E_local=8, topk=4, dtype="fp8", layout="compact", drop_every=5),
+    dict(T=1100, K=256, I=256, E_global=16, E_local=4, topk=4, dtype="fp8", layout="masked", expert_start=4),
+    dict(T=700, K=384, I=256, E_global=8, E_local=8, topk=4, dtype="mxfp8", layout="compact", zipf_s=1.2),
     dict(T=600, K=512, I=256, E_global=32, E_local=32, topk=8, dtype="fp8", layout="compact", zipf_s=1.2),
     # masked decode-sized blocks: max_m = 48, one partial block per expert
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
