@@ -25,8 +25,10 @@ struct moe_ctx {
   int device;
   int num_sms;
   moe_ws_layout_t ws;
-  CUtensorMap map_w13;
-  CUtensorMap map_w2;
+  CUtensorMap map_w13;      // [E][gate, up][I/128][128][K]: one box = a GEMM1 tile's gate and up rows
+  CUtensorMap map_w2;       // [E][K][I], 256-row boxes
+  CUtensorMap map_w13_sf;   // MX: packed scale chunks as [E][gate, up][I/128][K/128][512 B]
+  CUtensorMap map_w2_sf;    // MX: packed scale chunks as [E][K/128][I/128][512 B], two blocks per box
   // descriptors of the workspace activations, rebuilt when ws moves
   const void* ws_for_maps;
   CUtensorMap map_a;
@@ -77,6 +79,64 @@ moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim
                   packed4 ? CU_TENSOR_MAP_SWIZZLE_NONE : (store64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B),
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// A tiled map of rank 2..5: dims[0] innermost (elements, contiguous),
+// strides[i] the byte stride of dims[i + 1].
+moe_status_t make_map_nd(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Weight maps.  GEMM1's B tile (gate rows nb*128.. and up rows I + nb*128..)
+// is one box of the 5-d view [E][2][I/128][128][K]; GEMM2's (256 rows) one
+// box of [E][K][I].  MXFP4 rows are packed (two codes per byte), unswizzled.
+moe_status_t make_weight_maps(moe_ctx* c, const void* w13, const void* w2) {
+  const moe_shape_t& s = *&c->shape;
+  const uint64_t wd = c->fp4 ? 2 : 1, es = c->fp8 ? 1 : 2, E = static_cast<uint64_t>(s.E_local);
+  const CUtensorMapDataType dt = c->fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = c->fp4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint32_t inner = static_cast<uint32_t>((c->fp4 ? 64 : 128) / es);
+  const uint64_t K = static_cast<uint64_t>(s.K), I = static_cast<uint64_t>(s.I);
+  const uint64_t rb1 = K / wd * es;   // w13 row bytes
+  const uint64_t d1[5] = {K / wd, 128, I / 128, 2, E};
+  const uint64_t s1[4] = {rb1, 128 * rb1, I * rb1, 2 * I * rb1};
+  const uint32_t b1[5] = {inner, 128, 1, 2, 1};
+  moe_status_t st = make_map_nd(&c->map_w13, w13, dt, 5, d1, s1, b1, sw);
+  if (st != MOE_OK) return st;
+  const uint64_t rb2 = I / wd * es;   // w2 row bytes
+  const uint64_t d2[3] = {I / wd, K, E};
+  const uint64_t s2[2] = {rb2, K * rb2};
+  const uint32_t b2[3] = {inner, 256, 1};
+  st = make_map_nd(&c->map_w2, w2, dt, 3, d2, s2, b2, sw);
+  if (st != MOE_OK || !c->mx) return st;
+  // packed 512-byte scale chunks, chunk (e, row block b, K group k) at
+  // ((e * row_blocks + b) * k_groups + k) * 512, read as 128 x u32
+  const uint64_t kg1 = K / 128, kg2 = I / 128;
+  const uint64_t ds1[5] = {128, kg1, I / 128, 2, E};
+  const uint64_t ss1[4] = {512, kg1 * 512, (I / 128) * kg1 * 512, (2 * I / 128) * kg1 * 512};
+  const uint32_t bs1[5] = {128, 1, 1, 2, 1};
+  st = make_map_nd(&c->map_w13_sf, c->w13_sf, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, ds1, ss1, bs1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st != MOE_OK) return st;
+  const uint64_t ds2[4] = {128, kg2, K / 128, E};
+  const uint64_t ss2[3] = {512, kg2 * 512, (K / 128) * kg2 * 512};
+  const uint32_t bs2[4] = {128, 1, 2, 1};
+  return make_map_nd(&c->map_w2_sf, c->w2_sf, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, ds2, ss2, bs2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 moe_status_t check_shape(const moe_shape_t* s) {
@@ -265,9 +325,7 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
     return MOE_ERR_CUDA;
   }
   compute_ws_layout(c);
-  const int64_t wd = fp4 ? 2 : 1;   // MXFP4: two codes per byte along K
-  st = make_map(&c->map_w13, w13, fp8, shape->K / wd, 2 * shape->I, shape->E_local, fp4);
-  if (st == MOE_OK) st = make_map(&c->map_w2, w2, fp8, shape->I / wd, shape->K, shape->E_local, fp4);
+  st = make_weight_maps(c, w13, w2);
   if (st != MOE_OK) {
     delete c;
     return st;
@@ -356,10 +414,12 @@ static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
   int64_t max_tiles = ctx->ws.blocks * g.n_blocks;
   int grid = ctx->num_sms;
   if (max_tiles < grid) grid = static_cast<int>(max_tiles);
-  const CUtensorMap& a = stage == 1 ? ctx->map_a : ctx->map_h;
-  const CUtensorMap& b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
-  const CUtensorMap& out = stage == 1 ? ctx->map_a : ctx->map_y;   // stage 1 stores through plain writes
-  return cuda_status(moe::launch_gemm(g, a, b, out, grid, static_cast<cudaStream_t>(stream)));
+  moe::GemmMaps m;
+  m.a = stage == 1 ? ctx->map_a : ctx->map_h;
+  m.b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
+  m.out = stage == 1 ? ctx->map_a : ctx->map_y;   // stage 1 stores through plain writes
+  m.wsf = ctx->mx ? (stage == 1 ? ctx->map_w13_sf : ctx->map_w2_sf) : m.b;   // (not read without MX scales)
+  return cuda_status(moe::launch_gemm(g, m, grid, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_grouped_gemm_w13_act(moe_ctx* ctx, void* ws, void* stream) { return run_gemm(ctx, ws, stream, 1); }

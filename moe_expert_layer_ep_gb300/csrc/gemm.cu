@@ -71,8 +71,12 @@ __host__ __device__ constexpr int epi_warps(bool fp8, int stage, int fp4 = 0) {
   return (fp8 && stage == 1 && fp4 != 1) ? 8 : 4;
 }
 __host__ __device__ constexpr int conv_warps(int stage, int fp4) { return fp4 == 0 ? 0 : (stage == 1 && fp4 == 2 ? 2 : 4); }
-__host__ __device__ constexpr int threads_for(bool fp8, int stage, int fp4) {
-  return 64 + 32 * epi_warps(fp8, stage, fp4) + 32 * conv_warps(stage, fp4);
+// FP8 with 128x128 weight scales: one warp expands each stage's weight-scale
+// tile in shared memory, beside the TMA producer (whose loop then only
+// issues copies).
+__host__ __device__ constexpr int scale_warps(bool fp8, bool mx) { return fp8 && !mx ? 1 : 0; }
+__host__ __device__ constexpr int threads_for(bool fp8, bool mx, int stage, int fp4) {
+  return 64 + 32 * epi_warps(fp8, stage, fp4) + 32 * conv_warps(stage, fp4) + 32 * scale_warps(fp8, mx);
 }
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
@@ -169,10 +173,15 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
 
 __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
 
+// Tensor maps: map_a (A rows), map_b (weights; GEMM1 as [E][gate, up][I/128]
+// [128 rows][K] so that one box holds a tile's gate and up rows, GEMM2 in
+// 256-row boxes), map_out (GEMM2 y stores), map_wsf (MXFP8 weight-scale
+// chunks, both of a tile's chunks in one box).
 template <bool kFP8, bool kMX, int kStage, int kFP4>
-__global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
+__global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        const __grid_constant__ CUtensorMap map_out, const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_wsf,
+                        const GemmArgs g) {
   using L = Lay<(kFP4 != 0)>;
   constexpr int kStages = L::kStages;
   constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + scale_warps(kFP8, kMX));   // producer (+ scale warp)
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -216,6 +225,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
     fence_barrier_init();
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
+    if (kMX) prefetch_tensormap(&map_wsf);
   }
   if (warp == 1) {
     tmem_alloc(holder, kTmemCols);
@@ -242,19 +252,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
       int r0, r1;
       tile_b_rows<kStage>(g, tl, &r0, &r1);
       const int a_e = g.masked ? tl.expert : 0;
-      uint32_t sg_cache = 0, su_cache = 0;
       for (int kb = 0; kb < k_blocks; ++kb) {
-        if (kFP8 && !kMX && (kb & 31) == 0) {
-          // weight scales of the next 32 K blocks, one per lane
-          const int kk = kb + lane;
-          if (kk < k_blocks) {
-            const int b0 = min(r0 >> 7, g.w_rows_blocks - 1);
-            const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
-            const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
-            sg_cache = g.w_sf[(base + b0) * g.w_k_groups + kk];
-            su_cache = g.w_sf[(base + b1) * g.w_k_groups + kk];
-          }
-        }
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, g.timeout_ns);
         w_ok = __shfl_sync(0xFFFFFFFFu, w_ok, 0);
@@ -262,48 +260,35 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
           ok = false;
           break;
         }
-        if (kFP8 && !kMX) {
-          // B scale tile: 256 rows, rows 0..127 share the first block's scale,
-          // rows 128..255 the second's; 1 KB written by the warp.
-          const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, kb & 31);
-          const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, kb & 31);
-          const uint32_t word = (lane < 16 ? sg : su) * 0x01010101u;
-          uint4* dst = reinterpret_cast<uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane * 2;
-          dst[0] = make_uint4(word, word, word, word);
-          dst[1] = make_uint4(word, word, word, word);
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
         if (lane == 0) {
           const uint32_t bytes =
               kABytes + (kFP4 ? kBPBytes : kBBytes) + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kc = kb * kElemsPerKBlock;
           tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
-          if (kFP4) {
-            // packed E2M1 rows, 64 bytes per row per K block, unswizzled, into
-            // the upper half of the stage's B region (expanded in place)
-            uint8_t* bp = smem + kOffB + stage * kBBytes + kBBytes / 2;
-            tma_load_3d(bp, &map_b, &full[stage], kc / 2, r0, tl.expert);
-            tma_load_3d(bp + kBPBytes / 2, &map_b, &full[stage], kc / 2, r1, tl.expert);
-          } else {
-            tma_load_3d(smem + kOffB + stage * kBBytes, &map_b, &full[stage], kc, r0, tl.expert);
-            tma_load_3d(smem + kOffB + stage * kBBytes + kBBytes / 2, &map_b, &full[stage], kc, r1, tl.expert);
-          }
+          // the whole B tile in one box: GEMM1 gate rows then up rows, GEMM2
+          // 256 consecutive rows.  MXFP4: packed E2M1 rows, 64 bytes per row
+          // per K block, unswizzled, into the upper half of the stage's B
+          // region (expanded in place).
+          uint8_t* bdst = smem + kOffB + stage * kBBytes + (kFP4 ? kBBytes / 2 : 0);
+          const int kcb = kFP4 ? kc / 2 : kc;
+          if (kStage == 1)
+            tma_load_5d(bdst, &map_b, &full[stage], kcb, 0, tl.nb, 0, tl.expert);
+          else
+            tma_load_3d(bdst, &map_b, &full[stage], kcb, r0, tl.expert);
           if (kFP8) {
             bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + sf_chunk_offset(tl.sf_block, kb, k_blocks),
                       kSfaBytes, &full[stage]);
           }
           if (kMX) {
-            // B scale tile: the packed 512-byte chunks of the two 128-row
-            // weight blocks (rows past the end of w2 are TMA zeros, so the
-            // clamped chunk's scales multiply zeros)
-            const int b0 = min(r0 >> 7, g.w_rows_blocks - 1);
-            const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
-            const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
+            // B scale tile: the packed 512-byte chunks of the tile's two
+            // 128-row weight blocks in one box (a block past the end of w2
+            // reads as zeros: its weight rows are TMA zeros too)
             uint8_t* sfb = smem + kOffSfb + stage * kSfbBytes;
-            bulk_load(sfb, g.w_sf + sf_chunk_offset(base + b0, kb, g.w_k_groups), 512, &full[stage]);
-            bulk_load(sfb + 512, g.w_sf + sf_chunk_offset(base + b1, kb, g.w_k_groups), 512, &full[stage]);
+            if (kStage == 1)
+              tma_load_5d(sfb, &map_wsf, &full[stage], 0, kb, tl.nb, 0, tl.expert);
+            else
+              tma_load_4d(sfb, &map_wsf, &full[stage], 0, kb, 2 * tl.nb, tl.expert);
           }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -389,6 +374,57 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
       tc_commit(done);
       const int never = 0;
       mbar_wait_bounded(done, 0, &never, g.timeout_ns);
+    }
+  } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage, kFP4)) {
+    // ------------------------------------------------------------------ weight-scale tiles (FP8)
+    // B scale tile of each stage: 256 rows, rows 0..127 share the first
+    // weight block's scale, rows 128..255 the second's; 1 KB written by the
+    // warp, then its arrival completes the stage with the producer's copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const Tile tl = load_tile(g, t);
+      int r0, r1;
+      tile_b_rows<kStage>(g, tl, &r0, &r1);
+      const int b0 = min(r0 >> 7, g.w_rows_blocks - 1);
+      const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
+      const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
+      uint32_t sg_cache = 0, su_cache = 0;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if ((kb & 31) == 0) {
+          // weight scales of the next 32 K blocks, one per lane
+          const int kk = kb + lane;
+          if (kk < k_blocks) {
+            sg_cache = g.w_sf[(base + b0) * g.w_k_groups + kk];
+            su_cache = g.w_sf[(base + b1) * g.w_k_groups + kk];
+          }
+        }
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, g.timeout_ns);
+        w_ok = __shfl_sync(0xFFFFFFFFu, w_ok, 0);
+        if (!w_ok) {
+          ok = false;
+          break;
+        }
+        const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, kb & 31);
+        const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, kb & 31);
+        const uint32_t word = (lane < 16 ? sg : su) * 0x01010101u;
+        uint4* dst = reinterpret_cast<uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane * 2;
+        dst[0] = make_uint4(word, word, word, word);
+        dst[1] = make_uint4(word, word, word, word);
+        fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor-memory copy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (!ok) {
+      set_status(g.status, MOE_ERR_TIMEOUT);
+      *abort_flag = 1;
     }
   } else if (kFP4 && warp >= 2 + epi_warps(kFP8, kStage, kFP4)) {
     // ------------------------------------------------------------------ FP4 -> e4m3
@@ -715,8 +751,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kStage, kFP4), 1)
 }
 
 template <bool kFP8, bool kMX, int kStage, int kFP4 = 0>
-cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int grid,
-                       cudaStream_t s) {
+cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
   constexpr int kSmemBytes = Lay<(kFP4 != 0)>::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
@@ -725,7 +760,8 @@ cudaError_t launch_one(const GemmArgs& g, const CUtensorMap& a, const CUtensorMa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4><<<grid, threads_for(kFP8, kStage, kFP4), kSmemBytes, s>>>(a, b, out, g);
+  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>
+      <<<grid, threads_for(kFP8, kMX, kStage, kFP4), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
   return cudaGetLastError();
 }
 
@@ -747,21 +783,20 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 }  // namespace
 
 
-cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
   if (g.fp4) {
-    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, a, b, out, grid, s);
-    return g.masked ? launch_one<true, true, 1, 2>(g, a, b, out, grid, s) : launch_one<true, true, 1, 1>(g, a, b, out, grid, s);
+    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, m, grid, s);
+    return g.masked ? launch_one<true, true, 1, 2>(g, m, grid, s) : launch_one<true, true, 1, 1>(g, m, grid, s);
   }
   if (g.mx) {
-    return g.stage == 1 ? launch_one<true, true, 1>(g, a, b, out, grid, s) : launch_one<true, true, 2>(g, a, b, out, grid, s);
+    return g.stage == 1 ? launch_one<true, true, 1>(g, m, grid, s) : launch_one<true, true, 2>(g, m, grid, s);
   }
   if (g.fp8) {
-    return g.stage == 1 ? launch_one<true, false, 1>(g, a, b, out, grid, s)
-                        : launch_one<true, false, 2>(g, a, b, out, grid, s);
+    return g.stage == 1 ? launch_one<true, false, 1>(g, m, grid, s)
+                        : launch_one<true, false, 2>(g, m, grid, s);
   }
-  return g.stage == 1 ? launch_one<false, false, 1>(g, a, b, out, grid, s)
-                      : launch_one<false, false, 2>(g, a, b, out, grid, s);
+  return g.stage == 1 ? launch_one<false, false, 1>(g, m, grid, s)
+                      : launch_one<false, false, 2>(g, m, grid, s);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {

@@ -89,8 +89,15 @@ cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
 int plan_launch_count(int64_t A, int32_t E_local);   // kernels one launch_plan enqueues
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
-cudaError_t launch_gemm(const GemmArgs& g, const CUtensorMap& map_a, const CUtensorMap& map_b,
-                        const CUtensorMap& map_out, int grid, cudaStream_t s);
+// Tensor maps of one grouped-GEMM launch.
+struct GemmMaps {
+  CUtensorMap a;     // A rows (a or h)
+  CUtensorMap b;     // weights: w13 as [E][gate, up][I/128][128][K] (one box = a tile's gate and up
+                     // rows), w2 as [E][K][I] in 256-row boxes
+  CUtensorMap out;   // GEMM2: y, 32-column store boxes
+  CUtensorMap wsf;   // MXFP8 / MXFP4: packed weight-scale chunks, a tile's two chunks per box
+};
+cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& maps, int grid, cudaStream_t s);
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t s);
 cudaError_t launch_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,
