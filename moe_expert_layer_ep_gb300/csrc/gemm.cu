@@ -682,28 +682,58 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
         // thread stores the 128 x 32 tile; rows past the valid count land in
         // the expert's padding (compact) or are clipped at max_m by the map
         // (masked)).  Sparser blocks (decode) store their valid rows directly.
+        // FP8 (one accumulator): the thread first packs its whole row to
+        // bf16 in registers and frees the accumulator, so the next tile's MMAs
+        // do not wait for the stores.  BF16 (two accumulators) interleaves
+        // tensor-memory loads and stores chunk by chunk, and so does MXFP4
+        // (its converter warps leave no registers for the packed row).
+        constexpr bool kEarly = kFP8 && !kFP4;
         const int64_t col0 = static_cast<int64_t>(tl.nb) * kTileN;
         const bool use_tma = tl.valid >= kTileM / 2;     // uniform over the epilogue warps
         const bool issuer = warp == 2 && lane == 0;
         uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + col0;
         bool ok = true;
-#pragma unroll 1
-        for (int c = 0; c < kTileN / 32; ++c) {
-          uint32_t v32[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, v32);
-          tmem_ld_wait();
-          if (c == kTileN / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-          }
-          uint4 o[4];
+        uint32_t pk[kEarly ? kTileN / 2 : 1];
+        if constexpr (kEarly) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int b = v * 8;
-            o[v].x = pack_bf16x2(__uint_as_float(v32[b + 0]), __uint_as_float(v32[b + 1]));
-            o[v].y = pack_bf16x2(__uint_as_float(v32[b + 2]), __uint_as_float(v32[b + 3]));
-            o[v].z = pack_bf16x2(__uint_as_float(v32[b + 4]), __uint_as_float(v32[b + 5]));
-            o[v].w = pack_bf16x2(__uint_as_float(v32[b + 6]), __uint_as_float(v32[b + 7]));
+          for (int c = 0; c < kTileN / 32; c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, v0);
+            tmem_ld_32x32b_x32(taddr + (c + 1) * 32, v1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              pk[c * 16 + i] = pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+              pk[(c + 1) * 16 + i] = pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+        }
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) {
+          uint4 o[4];
+          if constexpr (kEarly) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              o[v] = make_uint4(pk[c * 16 + 4 * v], pk[c * 16 + 4 * v + 1], pk[c * 16 + 4 * v + 2],
+                                pk[c * 16 + 4 * v + 3]);
+          } else {
+            uint32_t v32[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, v32);
+            tmem_ld_wait();
+            if (c == kTileN / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(&tempty[acc]);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int b = v * 8;
+              o[v].x = pack_bf16x2(__uint_as_float(v32[b + 0]), __uint_as_float(v32[b + 1]));
+              o[v].y = pack_bf16x2(__uint_as_float(v32[b + 2]), __uint_as_float(v32[b + 3]));
+              o[v].z = pack_bf16x2(__uint_as_float(v32[b + 4]), __uint_as_float(v32[b + 5]));
+              o[v].w = pack_bf16x2(__uint_as_float(v32[b + 6]), __uint_as_float(v32[b + 7]));
+            }
           }
           if (!use_tma) {
             if (row_ok && col0 + c * 32 < g.n_total) {
