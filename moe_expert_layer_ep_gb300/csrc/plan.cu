@@ -147,35 +147,49 @@ __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
   __shared__ int s_warp[32];
   __shared__ int s_count[kMaxLocalExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // one warp per expert: exclusive scan of the expert's chunk counts (which
-  // become each chunk's offset inside the expert) and the expert total
-  // (up to 8 x 32 chunks of an expert are loaded together, so a warp waits
-  // for memory once per expert rather than once per 32 chunks)
-  constexpr int kLoads = 8;
-  for (int ex = warp; ex < p.E_local; ex += 32) {
-    int32_t* row = p.chunk_hist + static_cast<int64_t>(ex) * p.chunks;
-    int carry = 0;
+  // Warp w scans experts w, w + 32, w + 64, w + 96 (then the next four
+  // groups): the exclusive scan of an expert's chunk counts becomes each
+  // chunk's offset inside the expert, and its total the expert's count.
+  // The counts of all four experts for up to 8 x 32 chunks are loaded
+  // together, so the warp waits for memory once per 256 chunks rather than
+  // once per expert.
+  constexpr int kLoads = 8, kGroup = 4;
+  for (int ex0 = warp; ex0 < p.E_local; ex0 += 32 * kGroup) {
+    int carry[kGroup] = {0, 0, 0, 0};
     for (int c0 = 0; c0 < p.chunks; c0 += 32 * kLoads) {
-      int v[kLoads];
+      int v[kGroup][kLoads];
 #pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
-        const int c = c0 + 32 * j + lane;
-        v[j] = c < p.chunks ? row[c] : 0;
+      for (int g = 0; g < kGroup; ++g) {
+        const int ex = ex0 + 32 * g;
+        const int32_t* row = p.chunk_hist + static_cast<int64_t>(ex) * p.chunks;
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+          const int c = c0 + 32 * j + lane;
+          v[g][j] = (ex < p.E_local && c < p.chunks) ? row[c] : 0;
+        }
       }
 #pragma unroll
-      for (int j = 0; j < kLoads; ++j) {
-        const int c = c0 + 32 * j + lane;
-        int x = v[j];
+      for (int g = 0; g < kGroup; ++g) {
+        const int ex = ex0 + 32 * g;
+        if (ex >= p.E_local) continue;   // warp-uniform
+        int32_t* row = p.chunk_hist + static_cast<int64_t>(ex) * p.chunks;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-          if (lane >= o) x += y;
+        for (int j = 0; j < kLoads; ++j) {
+          const int c = c0 + 32 * j + lane;
+          int x = v[g][j];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (lane >= o) x += y;
+          }
+          if (c < p.chunks) row[c] = carry[g] + x - v[g][j];
+          carry[g] += __shfl_sync(0xFFFFFFFFu, x, 31);
         }
-        if (c < p.chunks) row[c] = carry + x - v[j];
-        carry += __shfl_sync(0xFFFFFFFFu, x, 31);
       }
     }
-    if (lane == 0) s_count[ex] = carry;
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g)
+      if (lane == 0 && ex0 + 32 * g < p.E_local) s_count[ex0 + 32 * g] = carry[g];
   }
   __syncthreads();
   expert_tables(p, s_count, s_warp, nullptr);
