@@ -33,12 +33,17 @@
 // MMA runs.
 //
 // One persistent CTA per SM:
-//   warp 0      TMA producer (A tile, B tiles, activation scale chunk; weight
-//               scales expanded into shared memory, or bulk-copied for MX)
+//   warp 0      TMA producer: per K block the A tile, the whole B tile in one
+//               box (GEMM1's gate and up rows through a 5-d view of w13) and
+//               the activation scale chunk (+ both MX weight-scale chunks in
+//               one box).  TMA accepts about 130 bytes per cycle per SM, so
+//               the producer's loop does nothing else.
 //   warp 1      TMEM allocation + single-thread MMA issue (tcgen05.cp of the
 //               scale tiles, 4 MMAs of K=32 bytes per 128-byte K block)
 //   epilogue    4 or 8 warps (see epi_warps): tcgen05.ld of the accumulator,
 //               then activation / quantisation and stores of valid rows
+//   scale warp  FP8 with 128x128 weight scales: expands each stage's weight
+//               scale tile in shared memory and arrives beside the producer
 //   converters  MXFP4 only, 2 or 4 warps (see conv_warps): FP4 -> e4m3
 // A 4-stage mbarrier ring connects producer and MMA; accumulator barriers
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
