@@ -141,8 +141,9 @@ int32_t moe_choose_layout(int32_t E_global, int32_t E_local);
  *         32-column block ([E_local, 2I, K/32] / [E_local, K, I/32]) in the
  *         packed order moe_pack_mx_scales writes (16-byte aligned)
  *   MXFP4: w13 uint8 [E_local, 2I, K/2], w2 uint8 [E_local, K, I/2]: E2M1 codes,
- *         two per byte, element 2j in the low nibble of byte j; scales as
- *         for MXFP8
+ *         two per byte, element 2j in the low nibble of byte j, 32-byte
+ *         aligned (else MOE_ERR_MISALIGNED; the GEMMs multiply the codes as
+ *         E2M1 operands without expanding them); scales as for MXFP8
  *   BF16: w13 bf16 [E_local, 2I, K], w2 bf16 [E_local, K, I]; w13_sf = w2_sf = NULL
  * Rows 0..I-1 of w13[e] are the gate projection W1, rows I..2I-1 the up
  * projection W3 [P2 "关键源码片段" deep_gemm.py: the activation splits the

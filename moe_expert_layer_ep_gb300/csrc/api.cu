@@ -103,22 +103,28 @@ moe_status_t make_map_nd(CUtensorMap* map, const void* base, CUtensorMapDataType
 
 // Weight maps.  GEMM1's B tile (gate rows nb*128.. and up rows I + nb*128..)
 // is one box of the 5-d view [E][2][I/128][128][K]; GEMM2's (256 rows) one
-// box of [E][K][I].  MXFP4 rows are packed (two codes per byte), unswizzled.
+// box of [E][K][I].  MXFP4 rows are packed (two codes per byte); the map
+// unpacks them into the shared-memory layout of an E2M1 MMA operand.
 moe_status_t make_weight_maps(moe_ctx* c, const void* w13, const void* w2) {
   const moe_shape_t& s = *&c->shape;
-  const uint64_t wd = c->fp4 ? 2 : 1, es = c->fp8 ? 1 : 2, E = static_cast<uint64_t>(s.E_local);
-  const CUtensorMapDataType dt = c->fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle sw = c->fp4 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
-  const uint32_t inner = static_cast<uint32_t>((c->fp4 ? 64 : 128) / es);
+  // MXFP4: the map counts 4-bit codes and unpacks each 16 of them into a
+  // 16-byte shared-memory group (the layout the MMA's E2M1 operand reads), so
+  // a 128-code box fills a 128-byte swizzled row as an FP8 box does.
+  const uint64_t es = c->fp8 ? 1 : 2, E = static_cast<uint64_t>(s.E_local);
+  const CUtensorMapDataType dt = c->fp4  ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B
+                                 : c->fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint32_t inner = static_cast<uint32_t>(128 / es);
   const uint64_t K = static_cast<uint64_t>(s.K), I = static_cast<uint64_t>(s.I);
-  const uint64_t rb1 = K / wd * es;   // w13 row bytes
-  const uint64_t d1[5] = {K / wd, 128, I / 128, 2, E};
+  const uint64_t rb1 = c->fp4 ? K / 2 : K * es;   // w13 row bytes
+  const uint64_t d1[5] = {K, 128, I / 128, 2, E};
   const uint64_t s1[4] = {rb1, 128 * rb1, I * rb1, 2 * I * rb1};
   const uint32_t b1[5] = {inner, 128, 1, 2, 1};
   moe_status_t st = make_map_nd(&c->map_w13, w13, dt, 5, d1, s1, b1, sw);
   if (st != MOE_OK) return st;
-  const uint64_t rb2 = I / wd * es;   // w2 row bytes
-  const uint64_t d2[3] = {I / wd, K, E};
+  const uint64_t rb2 = c->fp4 ? I / 2 : I * es;   // w2 row bytes
+  const uint64_t d2[3] = {I, K, E};
   const uint64_t s2[2] = {rb2, K * rb2};
   const uint32_t b2[3] = {inner, 256, 1};
   st = make_map_nd(&c->map_w2, w2, dt, 3, d2, s2, b2, sw);
@@ -300,6 +306,9 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   if (fp8 != (w13_sf != nullptr) || fp8 != (w2_sf != nullptr)) return MOE_ERR_DTYPE_MISMATCH;
   if (!aligned16(w13) || !aligned16(w2)) return MOE_ERR_MISALIGNED;
   if (mx && (!aligned16(w13_sf) || !aligned16(w2_sf))) return MOE_ERR_MISALIGNED;
+  // packed FP4 weights are read by TMA with 32-byte-aligned bases
+  if (fp4 && ((reinterpret_cast<uintptr_t>(w13) & 31u) || (reinterpret_cast<uintptr_t>(w2) & 31u)))
+    return MOE_ERR_MISALIGNED;
   int layout = shape->layout == MOE_LAYOUT_AUTO ? moe_choose_layout(shape->E_global, shape->E_local) : shape->layout;
   if (layout == MOE_LAYOUT_MASKED && shape->max_m < (shape->T > 0 ? shape->T : 1)) return MOE_ERR_INVALID_ARG;
   if (layout == MOE_LAYOUT_MASKED && static_cast<int64_t>(shape->E_local) * shape->max_m >= (int64_t(1) << 31))

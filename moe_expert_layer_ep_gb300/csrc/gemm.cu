@@ -28,9 +28,11 @@
 // 256 consecutive rows of w2.
 //
 // The MXFP4 variant (FP4 E2M1 weights with 1x32 scales, the FP4 item of
-// the same list) loads the packed weights into the upper half of each
-// stage's B region and expands them in place to e4m3 (exact) before the same
-// MMA runs.
+// the same list) is the MXFP8 kernel with an E2M1 B operand: the block-scaled
+// MMA multiplies e4m3 activations by E2M1 weights directly, and TMA unpacks
+// each 16 packed codes into the 16-byte shared-memory group that operand
+// reads (8 bytes of codes, 8 bytes of gap), so a B tile keeps the FP8 tile's
+// geometry while half as many bytes leave L2.
 //
 // One persistent CTA per SM:
 //   warp 0      TMA producer: per K block the A tile, the whole B tile in one
@@ -44,7 +46,6 @@
 //               then activation / quantisation and stores of valid rows
 //   scale warp  FP8 with 128x128 weight scales: expands each stage's weight
 //               scale tile in shared memory and arrives beside the producer
-//   converters  MXFP4 only, 2 or 4 warps (see conv_warps): FP4 -> e4m3
 // A 4-stage mbarrier ring connects producer and MMA; accumulator barriers
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
 // path, whose other tensor-memory columns hold the scale tiles).
@@ -64,40 +65,27 @@ namespace {
 // accumulator: its other tensor-memory columns hold the scale tiles) uses 8,
 // two per accumulator lane quadrant with half of the columns each, copies the
 // accumulator out and releases it before the activation and quantisation.
-// The others use 4 warps that interleave tensor-memory loads and stores
-// chunk by chunk (measured faster there).
-// MXFP4 weights add warps that expand the FP4 weights to e4m3 in shared
-// memory.  kFP4 = 1 (compact layouts, throughput): 4 epilogue warps (each
-// 32-column chunk of GEMM1 is one MXFP8 group of h) and 4 converter warps.
-// kFP4 = 2 (masked layouts, decode; GEMM1 only): the 8-warp early-release
-// epilogue and 2 converter warps (the register file allows no more).  Both
-// compute h with the same per-element operations, so they agree bitwise.
-__host__ __device__ constexpr int epi_warps(bool fp8, int stage, int fp4 = 0) {
-  return (fp8 && stage == 1 && fp4 != 1) ? 8 : 4;
-}
-__host__ __device__ constexpr int conv_warps(int stage, int fp4) { return fp4 == 0 ? 0 : (stage == 1 && fp4 == 2 ? 2 : 4); }
+// The others use 4 warps (measured faster there).
+__host__ __device__ constexpr int epi_warps(bool fp8, int stage) { return (fp8 && stage == 1) ? 8 : 4; }
 // FP8 with 128x128 weight scales: one warp expands each stage's weight-scale
 // tile in shared memory, beside the TMA producer (whose loop then only
 // issues copies).
 __host__ __device__ constexpr int scale_warps(bool fp8, bool mx) { return fp8 && !mx ? 1 : 0; }
-__host__ __device__ constexpr int threads_for(bool fp8, bool mx, int stage, int fp4) {
-  return 64 + 32 * epi_warps(fp8, stage, fp4) + 32 * conv_warps(stage, fp4) + 32 * scale_warps(fp8, mx);
+__host__ __device__ constexpr int threads_for(bool fp8, bool mx, int stage) {
+  return 64 + 32 * epi_warps(fp8, stage) + 32 * scale_warps(fp8, mx);
 }
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kKBlockBytes = 128;                  // one 128-byte swizzle atom of K per stage
 constexpr int kABytes = kTileM * kKBlockBytes;     // 16 KB
 constexpr int kBBytes = kTileN * kKBlockBytes;     // 32 KB
-constexpr int kBPBytes = kTileN * kKBlockBytes / 2;   // MXFP4: the packed B tile, 16 KB
+constexpr int kBPBytes = kTileN * kKBlockBytes / 2;   // MXFP4: the codes of a B tile, 16 KB (what its copy counts)
 constexpr int kSfaBytes = 512;
 constexpr int kSfbBytes = 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemCol = 256;               // FP8: scale tiles live in columns 256..383
 
-// Shared-memory map.  MXFP4 weights land packed in the upper half of the
-// stage's own B region and are expanded in place, so the FP4 pipeline keeps
-// the 4 stages of 48 KB.
-template <bool kFP4>
+// Shared-memory map.
 struct Lay {
   static constexpr int kStages = 4;
   static constexpr int kOffA = 0;
@@ -105,7 +93,7 @@ struct Lay {
   static constexpr int kOffSfa = kOffB + kStages * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kStages * kSfaBytes;
   static constexpr int kOffBar = kOffSfb + kStages * kSfbBytes;
-  static constexpr int kNumBars = 3 * kStages + 2 + 2 + 1 + 4 + 1 + 1;   // full, empty, conv; acc; done; amax; csync; esync
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 1 + 4 + 1;   // full, empty; acc; done; amax; esync
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffAmax = kOffAbort + 8;                 // 2 x 4 x 2 x 32 floats
@@ -115,20 +103,6 @@ struct Lay {
   static constexpr int kSmemBytes = kOffStage + 2 * kStageTileBytes + 1024;   // + 1024-byte alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
-
-// Eight E2M1 codes (one 32-bit word, element order from the low nibble) ->
-// eight e4m3 bytes (*lo: elements 0..3, *hi: 4..7).  The magnitudes 0, 0.5,
-// 1, 1.5, 2, 3, 4, 6 are e4m3 0x00 0x30 0x38 0x3C 0x40 0x44 0x48 0x4C, picked
-// with a byte permute on the low three bits of each nibble.  The sign: a
-// nibble with bit 3 set becomes selector 12 (sign-replicate of a 0x80 byte,
-// i.e. 0xFF), one without becomes 0 (a zero byte); masked to bit 7.  Exact:
-// every E2M1 value is an e4m3 value.
-__device__ __forceinline__ void fp4x8_to_e4m3(uint32_t w, uint32_t* lo, uint32_t* hi) {
-  const uint32_t m = w & 0x77777777u;
-  const uint32_t sg = (w & 0x88888888u) | ((w >> 1) & 0x44444444u);
-  *lo = __byte_perm(0x3C383000u, 0x4C484440u, m) | (__byte_perm(0u, 0x80u, sg) & 0x80808080u);
-  *hi = __byte_perm(0x3C383000u, 0x4C484440u, m >> 16) | (__byte_perm(0u, 0x80u, sg >> 16) & 0x80808080u);
-}
 
 // Instruction descriptors (M = 128, N = 256, both operands K-major, fp32 D).
 constexpr uint32_t kIdescBF16 = (1u << 4)      // D format f32
@@ -182,12 +156,15 @@ __device__ __forceinline__ float silu_mul(float gate, float up) { return gate / 
 // [128 rows][K] so that one box holds a tile's gate and up rows, GEMM2 in
 // 256-row boxes), map_out (GEMM2 y stores), map_wsf (MXFP8 weight-scale
 // chunks, both of a tile's chunks in one box).
-template <bool kFP8, bool kMX, int kStage, int kFP4>
-__global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
+// kFP4: MXFP4 weights, an E2M1 B operand (with kFP8 and kMX).
+template <bool kFP8, bool kMX, int kStage, bool kFP4>
+__global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_wsf,
                         const GemmArgs g) {
-  using L = Lay<(kFP4 != 0)>;
+  using L = Lay;
+  // B operand format: e4m3, or E2M1 (code 5) for FP4 weights
+  constexpr uint32_t kIdescB = kIdescFP8 | (kFP4 ? (5u << 10) : 0u);
   constexpr int kStages = L::kStages;
   constexpr int kOffA = L::kOffA, kOffB = L::kOffB, kOffSfa = L::kOffSfa, kOffSfb = L::kOffSfb;
   constexpr int kOffBar = L::kOffBar, kOffHolder = L::kOffHolder, kOffAbort = L::kOffAbort, kOffAmax = L::kOffAmax;
@@ -201,9 +178,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint64_t* done = bars + 2 * kStages + 4;
   uint64_t* xchg = bars + 2 * kStages + 5;  // [4]: the two epilogue warps of a lane quadrant
-  uint64_t* conv = bars + 2 * kStages + 9;  // [kStages] MXFP4: B expanded to e4m3
-  uint64_t* csync = bars + 3 * kStages + 9; // MXFP4: all converter threads have read the packed tile
-  uint64_t* esync = bars + 3 * kStages + 10; // GEMM2: the epilogue warps have staged a chunk
+  uint64_t* esync = bars + 2 * kStages + 9; // GEMM2: the epilogue warps have staged a chunk
   uint32_t* holder = reinterpret_cast<uint32_t*>(smem + kOffHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
@@ -216,15 +191,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage, kFP4));
+      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage));
     }
     mbar_init(done, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&xchg[q], 64);
-    if (kFP4) {
-      for (int s = 0; s < kStages; ++s) mbar_init(&conv[s], 32 * conv_warps(kStage, kFP4));
-      mbar_init(csync, 32 * conv_warps(kStage, kFP4));
-    }
-    mbar_init(esync, 32 * epi_warps(kFP8, kStage, kFP4));
+    mbar_init(esync, 32 * epi_warps(kFP8, kStage));
     if (kStage == 2) prefetch_tensormap(&map_out);
     *abort_flag = 0;
     fence_barrier_init();
@@ -268,19 +239,18 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
         if (lane == 0) {
           const uint32_t bytes =
               kABytes + (kFP4 ? kBPBytes : kBBytes) + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
+          // (FP4: the unpacking copy leaves the 8-byte gaps of each 16-byte
+          // group unwritten and counts only the 16 KB of codes)
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kc = kb * kElemsPerKBlock;
           tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
           // the whole B tile in one box: GEMM1 gate rows then up rows, GEMM2
-          // 256 consecutive rows.  MXFP4: packed E2M1 rows, 64 bytes per row
-          // per K block, unswizzled, into the upper half of the stage's B
-          // region (expanded in place).
-          uint8_t* bdst = smem + kOffB + stage * kBBytes + (kFP4 ? kBBytes / 2 : 0);
-          const int kcb = kFP4 ? kc / 2 : kc;
+          // 256 consecutive rows (MXFP4: the map counts 4-bit codes)
+          uint8_t* bdst = smem + kOffB + stage * kBBytes;
           if (kStage == 1)
-            tma_load_5d(bdst, &map_b, &full[stage], kcb, 0, tl.nb, 0, tl.expert);
+            tma_load_5d(bdst, &map_b, &full[stage], kc, 0, tl.nb, 0, tl.expert);
           else
-            tma_load_3d(bdst, &map_b, &full[stage], kcb, r0, tl.expert);
+            tma_load_3d(bdst, &map_b, &full[stage], kc, r0, tl.expert);
           if (kFP8) {
             bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + sf_chunk_offset(tl.sf_block, kb, k_blocks),
                       kSfaBytes, &full[stage]);
@@ -334,8 +304,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTileN);
         for (int kb = 0; kb < k_blocks; ++kb) {
-          // MXFP4: the converter warps signal once B is e4m3 (after the TMA landed)
-          if (!mbar_wait_bounded(kFP4 ? &conv[stage] : &full[stage], phase, abort_flag, g.timeout_ns)) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, g.timeout_ns)) {
             ok = false;
             break;
           }
@@ -355,8 +324,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
-                                   kMX ? (kIdescFP8 | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4))
-                                       : kIdescFP8,
+                                   kMX ? (kIdescB | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4))
+                                       : kIdescB,
                                    sfa_t, sfb_t, (kb | k) != 0);
           } else {
 #pragma unroll
@@ -380,7 +349,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
       const int never = 0;
       mbar_wait_bounded(done, 0, &never, g.timeout_ns);
     }
-  } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage, kFP4)) {
+  } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage)) {
     // ------------------------------------------------------------------ weight-scale tiles (FP8)
     // B scale tile of each stage: 256 rows, rows 0..127 share the first
     // weight block's scale, rows 128..255 the second's; 1 KB written by the
@@ -431,70 +400,13 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
       set_status(g.status, MOE_ERR_TIMEOUT);
       *abort_flag = 1;
     }
-  } else if (kFP4 && warp >= 2 + epi_warps(kFP8, kStage, kFP4)) {
-    // ------------------------------------------------------------------ FP4 -> e4m3
-    // Each stage's packed B tile (256 rows x 64 bytes, in the upper half of
-    // the B region) becomes the e4m3 B tile over the whole region (two
-    // 128-row boxes of 128-byte rows, 128-byte swizzle: 16-byte chunk c of row
-    // r at r * 128 + ((c ^ (r % 8)) * 16)).  The output overwrites packed
-    // bytes, so every converter thread first reads its share into registers
-    // and the converter warps meet on an mbarrier before anyone writes.
-    constexpr int kConv = conv_warps(kStage, kFP4) > 0 ? conv_warps(kStage, kFP4) : 1;   // (not FP4: unused)
-    constexpr int kChunks = kTileN * 8 / (32 * kConv);   // 16-byte output chunks per thread
-    const int ct = threadIdx.x - 32 * (2 + epi_warps(kFP8, kStage, kFP4));
-    int stage = 0;
-    uint32_t phase = 0, sync_phase = 0;
-    bool ok = true;
-    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        const bool got = mbar_wait_bounded(&full[stage], phase, abort_flag, g.timeout_ns);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
-          ok = false;
-          break;
-        }
-        uint8_t* dst = smem + kOffB + stage * kBBytes;
-        const uint8_t* src = dst + kBBytes / 2;
-        uint2 pk[kChunks];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-          const int q = ct + i * 32 * kConv;
-          pk[i] = *reinterpret_cast<const uint2*>(src + (q >> 3) * 64 + (q & 7) * 8);
-        }
-        mbar_arrive(csync);
-        const bool met = mbar_wait_bounded(csync, sync_phase, abort_flag, g.timeout_ns);
-        sync_phase ^= 1;
-        if (!__all_sync(0xFFFFFFFFu, met)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i) {
-          const int q = ct + i * 32 * kConv;
-          const int row = q >> 3, c = q & 7;
-          uint4 o;
-          fp4x8_to_e4m3(pk[i].x, &o.x, &o.y);
-          fp4x8_to_e4m3(pk[i].y, &o.z, &o.w);
-          *reinterpret_cast<uint4*>(dst + (row >> 7) * (kBBytes / 2) + (row & 127) * 128 + ((c ^ (row & 7)) << 4)) = o;
-        }
-        fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor cores
-        mbar_arrive(&conv[stage]);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
-    if (!ok) {
-      set_status(g.status, MOE_ERR_TIMEOUT);
-      *abort_flag = 1;
-    }
   } else {
     // ------------------------------------------------------------------ epilogue
     // Eight warps: two per tensor-memory lane quadrant (warp % 4), each
     // owning half of the tile's columns.  A thread copies its accumulator
     // slice to registers and releases the accumulator before any math, so
     // the next tile's MMAs never wait on activation, quantisation or stores.
-    constexpr int kEpiWarps = epi_warps(kFP8, kStage, kFP4);
+    constexpr int kEpiWarps = epi_warps(kFP8, kStage);
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;  // 0 when there are four epilogue warps
     const int r = quad * 32 + lane;
@@ -517,50 +429,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
       const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kTileN) + (static_cast<uint32_t>(quad * 32) << 16);
       const bool row_ok = r < tl.valid;
       const int64_t row = tl.row0 + r;
-      if (kStage == 1 && kEpiWarps == 4 && kFP8) {
-        // MXFP4 weights: h in MXFP8, each 32-column chunk one scale group
-        uint8_t* dst = static_cast<uint8_t*>(g.out) + row * g.out_ld + tl.nb * 128;
-        uint32_t sfw = 0;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t gv[32], uv[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, gv);
-          tmem_ld_32x32b_x32(taddr + 128 + c * 32, uv);
-          tmem_ld_wait();
-          if (c == 3) {
-            tc_fence_before();
-            mbar_arrive(&tempty[acc]);
-          }
-          float h[32];
-          float amax = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            h[i] = silu_mul(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
-            amax = fmaxf(amax, fabsf(h[i]));
-          }
-          const int s = ue8m0_exponent(amax);
-          const float mul = exp2_neg(s);
-          sfw |= static_cast<uint32_t>(s + 127) << (8 * c);
-          if (row_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-              const int b = 16 * v;
-              uint4 o;
-              o.x = cvt_e4m3x2(h[b + 0] * mul, h[b + 1] * mul) | (cvt_e4m3x2(h[b + 2] * mul, h[b + 3] * mul) << 16);
-              o.y = cvt_e4m3x2(h[b + 4] * mul, h[b + 5] * mul) | (cvt_e4m3x2(h[b + 6] * mul, h[b + 7] * mul) << 16);
-              o.z = cvt_e4m3x2(h[b + 8] * mul, h[b + 9] * mul) |
-                    (cvt_e4m3x2(h[b + 10] * mul, h[b + 11] * mul) << 16);
-              o.w = cvt_e4m3x2(h[b + 12] * mul, h[b + 13] * mul) |
-                    (cvt_e4m3x2(h[b + 14] * mul, h[b + 15] * mul) << 16);
-              d4[v] = o;
-            }
-          }
-        }
-        if (row_ok)
-          *reinterpret_cast<uint32_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
-                                       sf_row_offset(r)) = sfw;
-      } else if (kStage == 1 && kEpiWarps == 4) {
+      if (kStage == 1 && kEpiWarps == 4) {
         uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -690,9 +559,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
         // FP8 (one accumulator): the thread first packs its whole row to
         // bf16 in registers and frees the accumulator, so the next tile's MMAs
         // do not wait for the stores.  BF16 (two accumulators) interleaves
-        // tensor-memory loads and stores chunk by chunk, and so does MXFP4
-        // (its converter warps leave no registers for the packed row).
-        constexpr bool kEarly = kFP8 && !kFP4;
+        // tensor-memory loads and stores chunk by chunk.
+        constexpr bool kEarly = kFP8;
         const int64_t col0 = static_cast<int64_t>(tl.nb) * kTileN;
         const bool use_tma = tl.valid >= kTileM / 2;     // uniform over the epilogue warps
         const bool issuer = warp == 2 && lane == 0;
@@ -785,9 +653,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kFP4), 1)
   }
 }
 
-template <bool kFP8, bool kMX, int kStage, int kFP4 = 0>
+template <bool kFP8, bool kMX, int kStage, bool kFP4 = false>
 cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
-  constexpr int kSmemBytes = Lay<(kFP4 != 0)>::kSmemBytes;
+  constexpr int kSmemBytes = Lay::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>,
@@ -796,7 +664,7 @@ cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStrea
     attr_set = true;
   }
   grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>
-      <<<grid, threads_for(kFP8, kMX, kStage, kFP4), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
+      <<<grid, threads_for(kFP8, kMX, kStage), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
   return cudaGetLastError();
 }
 
@@ -819,10 +687,8 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 
 
 cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
-  if (g.fp4) {
-    if (g.stage == 2) return launch_one<true, true, 2, 1>(g, m, grid, s);
-    return g.masked ? launch_one<true, true, 1, 2>(g, m, grid, s) : launch_one<true, true, 1, 1>(g, m, grid, s);
-  }
+  if (g.fp4)
+    return g.stage == 1 ? launch_one<true, true, 1, true>(g, m, grid, s) : launch_one<true, true, 2, true>(g, m, grid, s);
   if (g.mx) {
     return g.stage == 1 ? launch_one<true, true, 1>(g, m, grid, s) : launch_one<true, true, 2>(g, m, grid, s);
   }

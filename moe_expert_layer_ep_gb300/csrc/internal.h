@@ -67,7 +67,7 @@ struct GemmArgs {
   int32_t stage;              // 1: w13 + SiLU*up, 2: w2
   int32_t fp8;
   int32_t mx;                 // fp8 with 1x32 scales; w_sf in the packed chunk order
-  int32_t fp4;                // mx with FP4 (E2M1) weights, packed two per byte, expanded to e4m3 in the kernel
+  int32_t fp4;                // mx with FP4 (E2M1) weights, packed two per byte: an E2M1 MMA operand
   int32_t masked;
   int32_t blocks_per_expert;  // masked
   int32_t n_blocks;           // output column blocks (128 h columns, or 256 y columns)

@@ -9,6 +9,8 @@ MXFP8 cases too):
   block or the wrong weight row changes the result.
 """
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -90,3 +92,17 @@ def test_gemm2_mx_scales_exact(layout):
     # y[row, n] = sum_c 32 * 2^(sh[row, c] + sw[e, n, c])
     expect = oracle.bf16_round(32.0 * np.einsum("rc,rnc->rn", np.exp2(sh), np.exp2(sw[expert])))
     assert np.array_equal(y, expect), np.count_nonzero(y != expect)
+
+
+def test_mxfp4_weights_need_32_byte_alignment():
+    # packed E2M1 weights are read by TMA copies that require 32-byte-aligned
+    # bases; a 16-byte-aligned pointer is rejected at context creation
+    p = Problem(T=16, K=256, I=128, E_global=8, E_local=8, topk=2, dtype="mxfp4", layout="compact",
+                weight_device="cuda")
+    g = p.gpu()   # packs the scales as the context expects them
+    shape = M.make_shape(16, 256, 128, 8, 8, 2, "mxfp4", "compact")
+    handle = ctypes.c_void_p()
+    for w13_off, w2_off in ((16, 0), (0, 16)):
+        code = M._lib.moe_ctx_create(ctypes.byref(shape), g.w13.data_ptr() + w13_off, g.w13_sf.data_ptr(),
+                                     g.w2.data_ptr() + w2_off, g.w2_sf.data_ptr(), ctypes.byref(handle))
+        assert code == M.STATUS["MOE_ERR_MISALIGNED"]
