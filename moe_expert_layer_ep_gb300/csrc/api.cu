@@ -62,21 +62,19 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // 3-D K-major tile map over [dim2][dim1][dim0] with a 128-byte inner box and
 // 128 rows, 128-byte swizzle (the layout the MMA descriptors expect).
-// packed4: byte rows of packed FP4 codes, a 64-byte inner box, no swizzle
-// (the kernel expands them into the swizzled e4m3 layout itself).
 // store64: a 64-byte inner box with 64-byte swizzle (the GEMM2 output stores).
 moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-                      bool packed4 = false, bool store64 = false) {
+                      bool store64 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
   const uint64_t esize = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
   cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>((packed4 || store64 ? 64 : 128) / esize), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>((store64 ? 64 : 128) / esize), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  packed4 ? CU_TENSOR_MAP_SWIZZLE_NONE : (store64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B),
+                  store64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -106,7 +104,7 @@ moe_status_t make_map_nd(CUtensorMap* map, const void* base, CUtensorMapDataType
 // box of [E][K][I].  MXFP4 rows are packed (two codes per byte); the map
 // unpacks them into the shared-memory layout of an E2M1 MMA operand.
 moe_status_t make_weight_maps(moe_ctx* c, const void* w13, const void* w2) {
-  const moe_shape_t& s = *&c->shape;
+  const moe_shape_t& s = c->shape;
   // MXFP4: the map counts 4-bit codes and unpacks each 16 of them into a
   // 16-byte shared-memory group (the layout the MMA's E2M1 operand reads), so
   // a 128-code box fills a 128-byte swizzled row as an FP8 box does.
@@ -230,7 +228,7 @@ moe_status_t ensure_ws_maps(moe_ctx* c, void* ws) {
     if (st != MOE_OK) return st;
     st = make_map(&c->map_h, at<uint8_t>(ws, c->ws.h), c->fp8, s.I, d1, d2);
     if (st != MOE_OK) return st;
-    st = make_map(&c->map_y, at<uint8_t>(ws, c->ws.y), false, s.K, d1, d2, false, true);
+    st = make_map(&c->map_y, at<uint8_t>(ws, c->ws.y), false, s.K, d1, d2, true);
     if (st != MOE_OK) return st;
   }
   c->ws_for_maps = ws;
