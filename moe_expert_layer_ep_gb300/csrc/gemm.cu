@@ -18,7 +18,8 @@
 // standard-dispatch report's "风险与影响" item 5) hands each 32-element
 // sub-block its own scale byte: the k-th MMA of a 128-byte K block reads byte
 // k of the scale words (scale-factor ID k), and the weight scales arrive as
-// packed chunks by bulk copy instead of being expanded in shared memory.
+// packed chunks (both of a tile's in one TMA box) instead of being expanded
+// in shared memory.
 //
 // Work unit: one 128-row expert block (from the block table written by the
 // plan) x one output column block.  Stage 1's B tile is 128 gate rows of w13
