@@ -63,3 +63,12 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["n_gpus"] == 2
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the rest of the line's contract: the metric and unit of the arm it is
+    # compared with, the workload it sampled, and a CPU baseline that is the
+    # line's own value
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["steps"] == 1 and d["warmup"] == 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "tiny_fp8" and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["value"] == d["value"] and cb["unit"] == "tokens/s" and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
