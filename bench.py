@@ -28,7 +28,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from moe_expert_layer_ep_gb300 import synth  # noqa: E402
+import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s, grouped-GEMM TFLOPS & % of roofline on 1xGB300"
 

@@ -196,8 +196,11 @@ typedef struct {
  * T * topk = 65536 with 256 local experts); larger problems return
  * MOE_ERR_BUFFER_TOO_SMALL.  Allocates nothing (no cudaMalloc/cudaFree or
  * allocating library call).  The first call on a device looks up the
- * array's device address; make it before any stream capture.  Calls share
- * the array: calls that overlap on the GPU race on it. */
+ * array's device address; make it before any stream capture.  The address is
+ * cached per device and assumes the primary context is not reset
+ * (cudaDeviceReset) while the library is loaded.  Calls share the array:
+ * calls that overlap on the GPU race on it.  Masked layouts need
+ * E_local * max_m < 2^31 (MOE_ERR_UNSUPPORTED otherwise). */
 moe_status_t moe_plan_layout_noalloc(const moe_shape_t* shape, const int32_t* topk_ids,
                                      const moe_plan_outputs_t* out, void* stream);
 

@@ -14,11 +14,13 @@
 // The kernels are the ones moe_plan_layout launches; only the scratch
 // pointers differ.  The first call on a device looks up the array's device
 // address (cudaGetSymbolAddress, with that device current) and caches it, so
-// make that first call before any stream capture.  All calls share the one
-// array, which keeps the contents of the last call: every scratch word is
-// written before it is read within a call, so nothing needs clearing, but
-// calls whose kernels overlap on the GPU (different streams, no ordering)
-// race on it.
+// make that first call before any stream capture.  The cached address
+// belongs to the device's primary context and stays valid as long as that
+// context is not reset (cudaDeviceReset) while the library is loaded.  All
+// calls share the one array, which keeps the contents of the last call:
+// every scratch word is written before it is read within a call, so nothing
+// needs clearing, but calls whose kernels overlap on the GPU (different
+// streams, no ordering) race on it.
 #include <mutex>
 
 #include "../../include/moe.h"
@@ -73,6 +75,8 @@ extern "C" moe_status_t moe_plan_layout_noalloc(const moe_shape_t* s, const int3
   if (layout != MOE_LAYOUT_COMPACT && layout != MOE_LAYOUT_MASKED) return MOE_ERR_INVALID_ARG;
   const bool masked = layout == MOE_LAYOUT_MASKED;
   if (masked && s->max_m < (s->T > 0 ? s->T : 1)) return MOE_ERR_INVALID_ARG;
+  // masked row offsets e * max_m + pos are int32 in the outputs
+  if (masked && static_cast<int64_t>(s->E_local) * s->max_m >= (int64_t(1) << 31)) return MOE_ERR_UNSUPPORTED;
 
   const int64_t A = s->T * s->topk;
   const int64_t chunks = (A + moe::kPlanChunk - 1) / moe::kPlanChunk;

@@ -6,7 +6,7 @@ import numpy as np
 import torch
 
 import oracle
-from moe_expert_layer_ep_gb300 import synth
+import synth
 
 
 def rel_fro(a, b):

@@ -49,3 +49,18 @@ def test_scale_chunk_offsets_are_a_bijection():
 def test_status_strings():
     for code in M.STATUS_NAMES:
         assert M._lib.moe_strerror(code)
+
+
+def test_noalloc_plan_rejects_masked_row_offsets_beyond_int32():
+    """The masked row of (expert e, position p) is e * max_m + p, stored as
+    int32: shapes where E_local * max_m reaches 2^31 are refused on the host,
+    before the device scratch is looked up or anything is launched."""
+    import ctypes
+    shape = M.make_shape(T=4, K=128, I=128, E_global=64, E_local=32, topk=2, dtype="fp8", layout="masked",
+                         max_m=1 << 26)                         # 32 * 2^26 = 2^31
+    outs = M.MoePlanOutputs()
+    code = M._lib.moe_plan_layout_noalloc(ctypes.byref(shape), None, ctypes.byref(outs), None)
+    assert code == M.STATUS["MOE_ERR_UNSUPPORTED"]
+    shape.max_m = (1 << 26) - 1                                 # fits: the next check (null outputs) answers
+    code = M._lib.moe_plan_layout_noalloc(ctypes.byref(shape), None, ctypes.byref(outs), None)
+    assert code == M.STATUS["MOE_ERR_INVALID_ARG"]

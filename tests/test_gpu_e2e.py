@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 import torch
 
-from moe_expert_layer_ep_gb300 import synth
+import synth
 from moe_testlib import Problem, bf16_to_f64, rel_fro
 
 pytestmark = pytest.mark.gpu

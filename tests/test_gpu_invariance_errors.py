@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import moe_expert_layer_ep_gb300 as M
-from moe_expert_layer_ep_gb300 import synth
+import synth
 from moe_testlib import Problem
 
 pytestmark = pytest.mark.gpu

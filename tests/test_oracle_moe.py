@@ -18,7 +18,7 @@ import torch
 
 import oracle
 from oracle import formats as F
-from moe_expert_layer_ep_gb300 import synth
+import synth
 
 
 def small_problem(dtype, T=40, K=256, I=256, E_global=6, E_local=4, expert_start=1, topk=3, seed=5):

@@ -15,7 +15,7 @@ import math
 import numpy as np
 
 import oracle
-from moe_expert_layer_ep_gb300 import synth
+import synth
 
 
 def test_e2m1_grid_from_format_parameters():

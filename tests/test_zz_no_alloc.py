@@ -19,7 +19,7 @@ import pytest
 import torch
 
 import moe_expert_layer_ep_gb300 as M
-from moe_expert_layer_ep_gb300 import synth
+import synth
 
 pytestmark = pytest.mark.gpu
 
@@ -48,12 +48,18 @@ def _outputs_like(ref):
     return {k: torch.full_like(v, -7) for k, v in ref.items()}
 
 
-@pytest.mark.parametrize("layout", ["compact", "masked"])
-def test_noalloc_plan_matches_workspace_plan_twice(layout):
-    if layout == "compact":
-        T, E_global, E_local, start, topk, zipf = 8192, 256, 256, 0, 8, 1.2
-    else:
-        T, E_global, E_local, start, topk, zipf = 256, 256, 32, 32, 8, None
+# (layout, T, E_global, E_local, expert_start, topk, Zipf exponent).  The
+# one-CTA plan serves up to 2048 assignments; the three-kernel plan, which
+# uses the static scratch array, serves larger problems, so the compact case
+# and the second masked case take that path.
+CASES = [("compact", 8192, 256, 256, 0, 8, 1.2),
+         ("masked", 256, 256, 32, 32, 8, None),
+         ("masked", 1024, 256, 32, 32, 8, None)]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-T{c[1]}" for c in CASES])
+def test_noalloc_plan_matches_workspace_plan_twice(case):
+    layout, T, E_global, E_local, start, topk, zipf = case
     shape = M.make_shape(T, 128, 128, E_global, E_local, topk, "fp8", layout, expert_start=start,
                          max_m=T if layout == "masked" else 0)
     for call in range(2):
