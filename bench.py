@@ -2,8 +2,10 @@
 
 One step = one moe_forward (plan -> quant/scatter -> GEMM1+act -> GEMM2 ->
 combine) over one batch of synthetic tokens already resident in HBM.  Default
-workload: the BF16 contiguous prefill (T=4096, K=2048, I=768, 128 experts,
-top-8).  Prints one JSON line (rank 0).
+workload: the FP8 block-quantised compact-layout prefill (T=8192, K=7168,
+I=2048, 256 experts, top-8, Zipf(1.2) expert popularity; e4m3 weights with
+128x128 UE8M0 scales, 1x128 UE8M0 activation scales).  Prints one JSON line
+(rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -38,7 +40,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="bf16_prefill", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="fp8_prefill_zipf", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--T", type=int, default=None, help="override the token count")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -168,10 +170,27 @@ def workload(args):
     return w
 
 
+def routing_seed(w):
+    """Routing seed of a workload: seed + 1, except that a workload holding
+    only some of the experts (a masked, expert-parallel slice) takes the
+    first of seed + 1, seed + 2, ... whose first token routes to at least one
+    local expert, so that every batch size, T = 1 included, runs the expert
+    GEMMs.  Token 0's logits do not depend on T, so neither does the seed."""
+    seed = w["seed"] + 1
+    if w["E_local"] == w["E_global"]:
+        return seed
+    es, El = w["expert_start"], w["E_local"]
+    while True:
+        ids, _ = synth.routing(1, w["E_global"], w["topk"], seed, w["zipf_s"])
+        if ((ids >= es) & (ids < es + El)).any():
+            return seed
+        seed += 1
+
+
 def build_inputs(w, device):
     T, K, I = w["T"], w["K"], w["I"]
     x = synth.activations(T, K, w["seed"], device)
-    ids, wts = synth.routing(T, w["E_global"], w["topk"], w["seed"] + 1, w["zipf_s"])
+    ids, wts = synth.routing(T, w["E_global"], w["topk"], routing_seed(w), w["zipf_s"])
     es = w["expert_start"]
     if w["dtype"] == "fp8":
         w13, w13s = synth.fp8_expert_weights(w["E_local"], 2 * I, K, w["seed"] + 2, device, es)
@@ -188,97 +207,193 @@ def build_inputs(w, device):
 
 
 def work_model(w, ids):
-    """Algorithmic work of one step (valid rows only)."""
-    T, K, I, E_l, es = w["T"], w["K"], w["I"], w["E_local"], w["expert_start"]
+    """Algorithmic work of one step (valid rows only).  Bytes count what the
+    method as described must move: the weights (and their scales) of the
+    non-empty experts once, the valid a / h / y rows written and read, x and
+    out; fused_bytes is the minimal fused bound (weights + x + out + routing)."""
+    T, K, I, E_l, es, k = w["T"], w["K"], w["I"], w["E_local"], w["expert_start"], w["topk"]
     ids = ids.numpy()
     loc = (ids >= es) & (ids < es + E_l)
     A = int(loc.sum())
     nonempty = len(np.unique(ids[loc]))
     esz = 1 if w["dtype"] in ("fp8", "mxfp8", "mxfp4") else 2    # activations and h
     wsz = 0.5 if w["dtype"] == "mxfp4" else esz                   # weights
+    # UE8M0 bytes per element: 1x128 activations / 128x128 weights, or 1x32 (MX)
+    asf = {"fp8": 1 / 128, "mxfp8": 1 / 32, "mxfp4": 1 / 32}.get(w["dtype"], 0.0)
+    wsf = {"fp8": 1 / 16384, "mxfp8": 1 / 32, "mxfp4": 1 / 32}.get(w["dtype"], 0.0)
     flops1 = 2.0 * A * K * 2 * I
     flops2 = 2.0 * A * I * K
-    w13_bytes = nonempty * 2 * I * K * wsz
-    w2_bytes = nonempty * K * I * wsz
-    # GEMM1 reads its weights, the valid a rows, writes h; GEMM2 likewise.
-    g1_bytes = w13_bytes + A * K * esz + A * I * esz
-    g2_bytes = w2_bytes + A * I * esz + A * K * 2
+    w13_bytes = nonempty * 2 * I * K * (wsz + wsf)
+    w2_bytes = nonempty * K * I * (wsz + wsf)
+    a_bytes = A * K * (esz + asf)
+    h_bytes = A * I * (esz + asf)
+    y_bytes = A * K * 2
+    # GEMM1 reads its weights and the valid a rows and writes h; GEMM2 reads
+    # its weights and h and writes y.
+    g1_bytes = w13_bytes + a_bytes + h_bytes
+    g2_bytes = w2_bytes + h_bytes + y_bytes
+    route = T * k * 8
     return {"A": A, "nonempty": nonempty, "flops1": flops1, "flops2": flops2, "g1_bytes": g1_bytes,
             "g2_bytes": g2_bytes, "weights_bytes": w13_bytes + w2_bytes,
-            "layer_bytes": w13_bytes + w2_bytes + T * K * 2 * 2 + 2 * A * K * esz + 2 * A * I * esz + 2 * A * K * 2}
+            "fused_bytes": w13_bytes + w2_bytes + 2 * T * K * 2 + route,
+            "layer_bytes": w13_bytes + w2_bytes + 2 * T * K * 2 + route + 2 * (a_bytes + h_bytes + y_bytes)}
 
 
-class OracleRunner:
-    """The fp64 oracle, as it stands, on a sample of the workload's tokens.
-    Expert weights are dequantised once, outside any timed region."""
+class OracleSample:
+    """The fp64 oracle, as it stands, timed on a bounded sample of a workload.
 
-    def __init__(self, w, x, ids, wts, weights):
+    Sample: the first ``n_tok`` tokens, and of their assignments those routed
+    to the ``n_exp`` local experts they use most (ties to the lower id); the
+    other assignments are dropped, as a rank holding only those experts drops
+    them.  One step is one ``oracle.forward_layout`` over that sample.  The
+    expert work is what dominates the layer, so the rate is reported per
+    assignment and scaled to tokens: tokens/s = assignments/s / topk.  Expert
+    weights are fetched and dequantised once, before any timed call.
+    """
+
+    def __init__(self, w, x, ids, wts, expert_fn, n_tok=256, n_exp=8):
         import oracle
-        self.oracle = oracle
-        self.w = w
-        self.x64 = x.float().cpu().numpy().astype(np.float64)
-        self.ids = ids.cpu().numpy()
-        self.wts = wts.cpu().numpy()
-        self.weights = tuple(t.cpu() if t is not None else None for t in weights)
-        self.cache = {}
-
-    def expert(self, e):
-        if e not in self.cache:
-            w13, w13s, w2, w2s = self.weights
-            if self.w["dtype"] in ("fp8", "mxfp8", "mxfp4"):
-                deq = {"fp8": self.oracle.dequant_fp8_weights, "mxfp8": self.oracle.dequant_mx_weights,
-                       "mxfp4": self.oracle.dequant_mxfp4_weights}[self.w["dtype"]]
-                a = deq(w13[e:e + 1].numpy(), w13s[e:e + 1].numpy().astype(np.int64) - 127)[0]
-                b = deq(w2[e:e + 1].numpy(), w2s[e:e + 1].numpy().astype(np.int64) - 127)[0]
+        self.oracle, self.w = oracle, w
+        T, k, es, El = w["T"], w["topk"], w["expert_start"], w["E_local"]
+        n_tok = min(T, n_tok)
+        ids = ids[:n_tok].cpu().numpy().astype(np.int64)
+        loc = ids - es
+        is_loc = (ids >= 0) & (loc >= 0) & (loc < El)
+        counts = np.bincount(loc[is_loc], minlength=El)
+        order = sorted(range(El), key=lambda e: (-counts[e], e))
+        chosen = sorted(e for e in order[:min(n_exp, El)] if counts[e] > 0)
+        remap = np.full(El, -1, dtype=np.int64)
+        remap[chosen] = np.arange(len(chosen))
+        self.ids = np.where(is_loc, remap[np.where(is_loc, loc, 0)], -1).astype(np.int32)
+        self.assignments = int((self.ids >= 0).sum())
+        self.x64 = x[:n_tok].float().cpu().numpy().astype(np.float64)
+        self.wts = wts[:n_tok].cpu().numpy()
+        self.n_tok, self.experts = n_tok, chosen
+        deq = []
+        for e in chosen:
+            w13, w13s, w2, w2s = expert_fn(e)
+            if w["dtype"] in ("fp8", "mxfp8", "mxfp4"):
+                f = {"fp8": oracle.dequant_fp8_weights, "mxfp8": oracle.dequant_mx_weights,
+                     "mxfp4": oracle.dequant_mxfp4_weights}[w["dtype"]]
+                deq.append((f(w13.numpy(), w13s.numpy().astype(np.int64) - 127)[0],
+                            f(w2.numpy(), w2s.numpy().astype(np.int64) - 127)[0]))
             else:
-                a = w13[e].float().numpy().astype(np.float64)
-                b = w2[e].float().numpy().astype(np.float64)
-            self.cache[e] = (a, b)
-        return self.cache[e]
+                deq.append((w13[0].float().numpy().astype(np.float64), w2[0].float().numpy().astype(np.float64)))
+        self.w13 = np.stack([d[0] for d in deq]) if deq else np.zeros((0, 2 * w["I"], w["K"]))
+        self.w2 = np.stack([d[1] for d in deq]) if deq else np.zeros((0, w["K"], w["I"]))
+
+    def describe(self):
+        w = self.w
+        return (f"first {self.n_tok} of {w['T']} tokens of workload {w['name']}, their {self.assignments} "
+                f"assignments to their {len(self.experts)} most-used local experts (the rest dropped); fp64 numpy "
+                f"oracle, layout path; tokens/s = assignments/s / topk")
+
+    def step(self):
+        t0 = time.perf_counter()
+        self.oracle.forward_layout(self.x64, self.w13, self.w2, self.ids, self.wts, self.w["dtype"],
+                                   E_global=max(1, len(self.experts)), layout="compact")
+        return time.perf_counter() - t0
 
     def run(self, seconds_target):
-        w = self.w
-        T, K, I = w["T"], w["K"], w["I"]
-        es, El = w["expert_start"], w["E_local"]
-        n, elapsed, chunk = 0, 0.0, 8
-        while n < T and elapsed < seconds_target:
-            sl = slice(n, min(T, n + chunk))
-            loc = sorted({int(i) - es for i in self.ids[sl].reshape(-1) if es <= int(i) < es + El})
-            w13d = np.stack([self.expert(e)[0] for e in loc]) if loc else np.zeros((0, 2 * I, K))
-            w2d = np.stack([self.expert(e)[1] for e in loc]) if loc else np.zeros((0, K, I))
-            remap = np.array([[loc.index(int(i) - es) if es <= int(i) < es + El else -1 for i in row]
-                              for row in self.ids[sl]])
-            t0 = time.perf_counter()
-            self.oracle.forward_layout(self.x64[sl], w13d, w2d, remap, self.wts[sl], w["dtype"],
-                                       E_global=max(1, len(loc)), layout="compact")
-            elapsed += time.perf_counter() - t0
-            n = sl.stop
-        return {"value": n / elapsed, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                "sample": f"first {n} of {T} tokens of workload {w['name']}, fp64 numpy oracle (layout path), "
-                          f"{elapsed:.1f} s", "tokens": n}
+        """Repeat the sample for about seconds_target of timed oracle work."""
+        elapsed, reps = 0.0, 0
+        while reps == 0 or elapsed < seconds_target:
+            elapsed += self.step()
+            reps += 1
+        value = reps * self.assignments / self.w["topk"] / elapsed
+        return {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"{self.describe()}; {reps} repetition(s), {elapsed:.1f} s"}
+
+
+def expert_source(w, weights=None):
+    """expert_fn(e) -> (w13, w13_sf, w2, w2_sf) CPU tensors of local expert e:
+    sliced from the device weights when given, else generated on the host
+    from the expert's own seed (synthetic weights are seeded per expert)."""
+    I, K, es = w["I"], w["K"], w["expert_start"]
+
+    def from_device(e):
+        return tuple(t[e:e + 1].cpu() if t is not None else None for t in weights)
+
+    def generated(e):
+        if w["dtype"] == "fp8":
+            gen = synth.fp8_expert_weights
+        elif w["dtype"] in ("mxfp8", "mxfp4"):
+            gen = synth.mxfp8_expert_weights if w["dtype"] == "mxfp8" else synth.mxfp4_expert_weights
+        else:
+            a = synth.bf16_expert_weights(1, 2 * I, K, w["seed"] + 2, "cpu", es + e)
+            b = synth.bf16_expert_weights(1, K, I, w["seed"] + 3, "cpu", es + e)
+            return a, None, b, None
+        a, sa = gen(1, 2 * I, K, w["seed"] + 2, "cpu", es + e)
+        b, sb = gen(1, K, I, w["seed"] + 3, "cpu", es + e)
+        return a, sa, b, sb
+
+    return from_device if weights is not None else generated
 
 
 def run_reference(args, w, world, rank):
     if rank != 0:
         return
-    x, ids, wts, weights = build_inputs(w, "cpu")
-    runner = OracleRunner(w, x, ids, wts, weights)
+    T, K = w["T"], w["K"]
+    x = synth.activations(T, K, w["seed"], "cpu")
+    ids, wts = synth.routing(T, w["E_global"], w["topk"], routing_seed(w), w["zipf_s"])
+    sample = OracleSample(w, x, ids, wts, expert_source(w))
     per_step = []
     for s in range(args.warmup + args.steps):
-        r = runner.run(seconds_target=2.0)
+        dt = sample.step()
         if s >= args.warmup:
-            per_step.append(r)
-    value = statistics.median(r["value"] for r in per_step)
-    n_tok = per_step[0]["tokens"]
+            per_step.append(dt)
+    elapsed = float(sum(per_step))
+    value = len(per_step) * sample.assignments / w["topk"] / elapsed
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * n_tok / value,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * elapsed / len(per_step),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w["name"], "T": w["T"], "K": w["K"], "I": w["I"],
                                             "E": w["E_local"], "topk": w["topk"]},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": per_step[0]["sample"]},
+                             "sample": sample.describe() + "; one sample per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def capture_graph(body, dev):
+    """A CUDA graph of body() (one side-stream pass first, as capture needs
+    the work to have run once outside it)."""
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body(warm=True)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        body(warm=False)
+    return graph
+
+
+def gemm_roofline(name, flops, nbytes, ms, peaks, fp8):
+    """Roofline of one GEMM launch: the bound is whichever of the tensor time
+    (algorithmic FLOPs at the dtype's peak) and the HBM time (algorithmic
+    bytes at the measured copy bandwidth) is larger."""
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    sec = ms / 1000.0
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (tensor_peak * 1e12)
+    gbs, tf = nbytes / sec / 1e9, flops / sec / 1e12
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": round(tf / tensor_peak, 4)}
+    roof.update({"kernel": name, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                 "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
+                 "tensor_frac": round(tf / tensor_peak, 4), "hbm_gbs": round(gbs, 1),
+                 "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                 "peak_source": peaks["source"] + (" (burst bf16 x 2 for fp8)" if fp8 else " (burst bf16)")})
+    return roof
+
+
+def pct(a, q):
+    return round(float(np.percentile(np.asarray(a), q)), 4)
 
 
 def run_ours(args, w, world, rank, local):
@@ -287,8 +402,9 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.set_device(dev)
     x, ids_host, w_host, weights = build_inputs(w, dev)
     ids, wts = ids_host.to(dev), w_host.to(dev)
+    max_m = w.get("max_m", 0) or (w["T"] if w["layout"] == "masked" else 0)
     shape = M.make_shape(w["T"], w["K"], w["I"], w["E_global"], w["E_local"], w["topk"], w["dtype"], w["layout"],
-                         w["expert_start"], w.get("max_m", 0) or (w["T"] if w["layout"] == "masked" else 0))
+                         w["expert_start"], max_m)
     ctx_weights = weights
     if w["dtype"] in ("mxfp8", "mxfp4"):   # the context takes packed MX scales; the oracle reads the natural ones
         ctx_weights = (weights[0], M.moe_pack_mx_scales(weights[1]), weights[2], M.moe_pack_mx_scales(weights[3]))
@@ -303,6 +419,8 @@ def run_ours(args, w, world, rank, local):
               lambda: M.moe_grouped_gemm_w13_act(ctx, ws),
               lambda: M.moe_grouped_gemm_w2(ctx, ws),
               lambda: M.moe_combine(ctx, wts, ws, out)]
+    names = ["plan", "quant_scatter", "gemm_w13_act", "gemm_w2", "combine"]
+    nst = len(stages)
     for _ in range(args.warmup):
         M.moe_forward(ctx, x, ids, wts, ws, out)
     torch.cuda.synchronize()
@@ -310,57 +428,76 @@ def run_ours(args, w, world, rank, local):
     if status != 0:
         raise RuntimeError(f"device status {M.STATUS_NAMES.get(status, status)} after warm-up")
 
-    # The timed region replays one CUDA graph holding args.steps forwards,
-    # with timing events recorded between the stages inside the graph (the
-    # layer is static-shape, so this is how it runs in production).  Without
-    # graph-capturable events the steps are launched eagerly instead.
-    nst = len(stages)
+    # The timed region replays graph A: args.steps forwards with one event at
+    # every step boundary (the layer is static-shape, so this is how it runs
+    # in production).  Graph B holds the same forwards with events between
+    # the stages as well; it gives the stage breakdown and stays out of the
+    # timed region, as its extra events cost time of their own.  Without
+    # graph-capturable events both are launched eagerly instead.
     timing = "cuda-graph replay"
-    try:
-        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nst + 1)]
-              for _ in range(args.steps)]
-        side = torch.cuda.Stream(device=dev)
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
+    step_ev = stage_ev = None
+
+    def body_a(warm):
+        for s in range(args.steps):
+            if not warm:
+                step_ev[s].record()
             M.moe_forward(ctx, x, ids, wts, ws, out)
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for s in range(args.steps):
-                ev[s][0].record()
-                for i, fn in enumerate(stages):
-                    fn()
-                    ev[s][i + 1].record()
-        graph.replay()                      # one untimed replay
-        torch.cuda.synchronize()
-        run_timed = graph.replay
+        if not warm:
+            step_ev[args.steps].record()
+
+    def body_b(warm):
+        for s in range(args.steps):
+            if not warm:
+                stage_ev[s][0].record()
+            for i, fn in enumerate(stages):
+                fn()
+                if not warm:
+                    stage_ev[s][i + 1].record()
+
+    try:
+        step_ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(args.steps + 1)]
+        stage_ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nst + 1)]
+                    for _ in range(args.steps)]
+        graph_a = capture_graph(body_a, dev)
+        graph_b = capture_graph(body_b, dev)
+        run_a, run_b = graph_a.replay, graph_b.replay
     except Exception:                        # events in graphs unsupported: eager launches
         timing = "eager launches"
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+        step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+        run_a, run_b = (lambda: body_a(False)), (lambda: body_b(False))
+    run_a()
+    run_b()
+    torch.cuda.synchronize()
 
-        def run_timed():
-            for s in range(args.steps):
-                ev[s][0].record(stream)
-                for i, fn in enumerate(stages):
-                    fn()
-                    ev[s][i + 1].record(stream)
+    def keep_busy(seconds):
+        """Untimed replays around the timed one, so that the clock samples
+        see the GPU under the same load."""
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            run_a()
+            torch.cuda.synchronize()
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        keep_busy(0.4)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        run_timed()
+        run_a()
         t1.record(stream)
         torch.cuda.synchronize()
+        step_ms = [step_ev[s].elapsed_time(step_ev[s + 1]) for s in range(args.steps)]
+        keep_busy(0.3)
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    stage_ms = np.array([[ev[s][i].elapsed_time(ev[s][i + 1]) for i in range(nst)]
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    run_b()
+    torch.cuda.synchronize()
+    stage_ms = np.array([[stage_ev[s][i].elapsed_time(stage_ev[s][i + 1]) for i in range(nst)]
                          for s in range(args.steps)])
-    total_ms = max_over_ranks(total_ms, world, dev)
 
     # end to end through the C-ABI with host buffers, as a serving loop runs
     # it: every step copies its x / ids / weights from pinned host memory and
@@ -428,30 +565,25 @@ def run_ours(args, w, world, rank, local):
     value = replica_value(T, world, args.steps, total_ms)
     med = np.median(stage_ms, axis=0)
     g1_ms, g2_ms = float(med[2]), float(med[3])
-    gemm_tflops = (wm["flops1"] + wm["flops2"]) / ((g1_ms + g2_ms) / 1000.0) / 1e12
     fp8 = w["dtype"] in ("fp8", "mxfp8", "mxfp4")
     tensor_peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
-    g1_gbs = wm["g1_bytes"] / (g1_ms / 1000.0) / 1e9
-    g1_tf = wm["flops1"] / (g1_ms / 1000.0) / 1e12
-    # dominant kernel: GEMM1; bound = whichever of its roofline times is larger
-    t_hbm = wm["g1_bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = wm["flops1"] / (tensor_peak * 1e12)
-    if t_hbm >= t_tc:
-        roof = {"bound": "hbm", "achieved": round(g1_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(g1_gbs / peaks["hbm_gbs"], 4)}
-    else:
-        roof = {"bound": "tensor", "achieved": round(g1_tf, 1), "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": round(g1_tf / tensor_peak, 4)}
+    gemm_tflops = (wm["flops1"] + wm["flops2"]) / ((g1_ms + g2_ms) / 1000.0) / 1e12
+    # dominant kernel: GEMM1; GEMM2 beside it
+    roof = gemm_roofline("grouped_gemm_kernel<stage 1> (moe_grouped_gemm_w13_act)", wm["flops1"], wm["g1_bytes"],
+                         g1_ms, peaks, fp8)
+    roof2 = gemm_roofline("grouped_gemm_kernel<stage 2> (moe_grouped_gemm_w2)", wm["flops2"], wm["g2_bytes"],
+                          g2_ms, peaks, fp8)
     # executed work: every row of the padded 128-row blocks goes through the MMAs
     padded_rows = int(M.ws_view(ctx, ws, "meta")[0].item())
-    exec_tf = 2.0 * padded_rows * w["K"] * 2 * w["I"] / (g1_ms / 1000.0) / 1e12
-    roof.update({"executed_tflops": round(exec_tf, 1), "executed_tensor_frac": round(exec_tf / tensor_peak, 4)})
-    roof.update({"kernel": "grouped_gemm_kernel<stage 1>",
-                 "traffic": measured_traffic(w["name"]) if not args.T else None,
-                 "algorithmic_bytes": int(wm["g1_bytes"]),
-                 "peak_source": peaks["source"] + (" (bf16 x 2 for fp8)" if fp8 else "")})
+    exec1 = 2.0 * padded_rows * w["K"] * 2 * w["I"] / (g1_ms / 1000.0) / 1e12
+    exec2 = 2.0 * padded_rows * w["I"] * w["K"] / (g2_ms / 1000.0) / 1e12
+    roof.update({"executed_tflops": round(exec1, 1), "executed_tensor_frac": round(exec1 / tensor_peak, 4),
+                 "traffic": measured_traffic(w["name"]) if not args.T else None})
+    roof2.update({"executed_tflops": round(exec2, 1), "executed_tensor_frac": round(exec2 / tensor_peak, 4)})
     layer_roof_ms = 1000.0 * max(wm["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
                                  (wm["flops1"] + wm["flops2"]) / (tensor_peak * 1e12))
+    fused_ms = 1000.0 * max(wm["fused_bytes"] / (peaks["hbm_gbs"] * 1e9),
+                            (wm["flops1"] + wm["flops2"]) / (tensor_peak * 1e12))
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
@@ -459,26 +591,35 @@ def run_ours(args, w, world, rank, local):
                   "mxfp4": "mxfp4-e2m1-weights/mxfp8-activations"}.get(w["dtype"], "bf16"),
         "data": "synthetic (seeded; random-init weights)",
         "config": {"workload": w["name"], "T": T, "K": w["K"], "I": w["I"], "E": w["E_local"],
-                   "topk": w["topk"], "layout": w["layout"], "l2": "weights larger than L2 (no flush needed)",
+                   "E_global": w["E_global"], "topk": w["topk"], "layout": w["layout"],
+                   **({"max_m": max_m} if w["layout"] == "masked" else {}),
+                   **({"zipf_s": w["zipf_s"]} if w["zipf_s"] else {}),
+                   "l2": "weights larger than L2 (no flush needed)" if wm["weights_bytes"] > 2 * 129e6
+                   else "L2 not flushed: weights fit in L2",
                    "parallelism": f"replicas x{world}", "timing": timing},
+        "step_ms_p10_p50_p90": [pct(step_ms, 10), pct(step_ms, 50), pct(step_ms, 90)],
         "gemm_tflops": round(gemm_tflops, 1),
         "layer_roofline_frac": round(layer_roof_ms / ms_per_step, 4),
-        "stage_ms": {n: round(float(v), 4) for n, v in zip(["plan", "quant_scatter", "gemm_w13_act", "gemm_w2",
-                                                            "combine"], med)},
+        "minimal_fused_bound": {"bytes": int(wm["fused_bytes"]), "ms": round(fused_ms, 4),
+                                "frac": round(fused_ms / ms_per_step, 4),
+                                "what": "weights of non-empty experts + x + out (+ routing) at the measured "
+                                        "HBM bandwidth, or the tensor time if larger"},
+        "stage_ms": {n: round(float(v), 4) for n, v in zip(names, med)},
+        "stage_ms_p10": {n: pct(stage_ms[:, i], 10) for i, n in enumerate(names)},
+        "stage_ms_p90": {n: pct(stage_ms[:, i], 90) for i, n in enumerate(names)},
         "roofline": roof,
+        "roofline_gemm2": roof2,
         "clocks": clk.summary(),
         "e2e": {"value": round(replica_value(T, world, args.steps, e2e_ms), 1), "unit": "tokens/s",
                 "pipelining": "h2d / d2h on copy streams overlapping the neighbouring steps' forwards",
                 "h2d_bytes_per_step": x.numel() * 2 + ids.numel() * 4 + wts.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2},
         "gpu_launches": M.moe_forward_launches(ctx) * args.steps,
-        "work": {"assignments": wm["A"], "nonempty_experts": wm["nonempty"],
-                 "padded_rows": int(M.ws_view(ctx, ws, "meta")[0].item())},
+        "work": {"assignments": wm["A"], "nonempty_experts": wm["nonempty"], "padded_rows": padded_rows},
     }
     if not args.no_cpu_baseline and world == 1:       # timed beside the N=1 line only
-        cb = OracleRunner(w, x, ids_host, w_host, weights).run(seconds_target=12.0)
-        cb.pop("tokens")
-        line["cpu_baseline"] = cb
+        sample = OracleSample(w, x, ids_host, w_host, expert_source(w, weights))
+        line["cpu_baseline"] = sample.run(seconds_target=12.0)
     print(json.dumps(line), flush=True)
 
 
