@@ -121,6 +121,15 @@ typedef struct {
   int64_t blocks;       /* static number of 128-row blocks */
   int32_t layout;       /* resolved moe_layout_t */
   int32_t chunks;       /* plan chunks of 256 assignments */
+  /* Masked layout only (0 / empty for compact): each expert GEMM's K loop runs
+   * in k_splits fixed segments (from K, I and the dtype alone, never from T or
+   * max_m); every segment writes fp32 partial sums of the tile's valid rows,
+   * and a second kernel of the same call adds them in segment order. */
+  uint64_t block_vrow;  /* int32[blocks]: first valid-row index of each block (rows counted without padding) */
+  uint64_t partial;     /* fp32 [k_splits][partial_rows][partial_cols] segment sums */
+  int64_t partial_rows; /* min(T * topk, E_local * max_m) */
+  int32_t k_splits1;    /* segments of GEMM1 (w13) */
+  int32_t k_splits2;    /* segments of GEMM2 (w2) */
 } moe_ws_layout_t;
 
 typedef struct moe_ctx moe_ctx;

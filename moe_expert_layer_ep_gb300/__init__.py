@@ -61,7 +61,9 @@ class MoePlanOutputs(ctypes.Structure):
 class MoeWsLayout(ctypes.Structure):
     _fields_ = [(f, ctypes.c_uint64) for f in _WS_FIELDS] + [
         ("rows", ctypes.c_int64), ("all_tokens", ctypes.c_int64), ("blocks", ctypes.c_int64),
-        ("layout", ctypes.c_int32), ("chunks", ctypes.c_int32)]
+        ("layout", ctypes.c_int32), ("chunks", ctypes.c_int32),
+        ("block_vrow", ctypes.c_uint64), ("partial", ctypes.c_uint64),
+        ("partial_rows", ctypes.c_int64), ("k_splits1", ctypes.c_int32), ("k_splits2", ctypes.c_int32)]
 
 
 def _load():

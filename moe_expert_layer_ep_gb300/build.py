@@ -12,7 +12,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "plan.cu", "quant.cu", "gemm.cu", "plan_noalloc.cu", "requant.cu", "router.cu"]
+SOURCES = ["api.cu", "plan.cu", "quant.cu", "gemm.cu", "split_reduce.cu", "plan_noalloc.cu", "requant.cu",
+           "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -160,6 +160,25 @@ moe_status_t check_shape(const moe_shape_t* s) {
   return MOE_OK;
 }
 
+// Segments of a masked-layout GEMM's K loop.  Chosen from the tile shape
+// alone (column tiles and K blocks, i.e. K, I and the dtype), never from T or
+// max_m, so that a token's sums are formed the same way at every batch size:
+// about 128 work units per expert (column tiles x segments), at least two K
+// blocks per segment and at most kMaxKSplits segments.  A GEMM whose experts
+// have 24 or more column tiles is not split: at the decode shapes (the w2
+// GEMM, 28 tiles of 256 columns) the split measured slower at every batch
+// size, while the w13 GEMM (16 tiles) gained.
+int k_splits_for(int64_t n_blocks, int64_t k_blocks) {
+  if (n_blocks >= 24) return 1;
+  int64_t s = 128 / (n_blocks > 0 ? n_blocks : 1);
+  if (s > k_blocks / 2) s = k_blocks / 2;
+  if (s > moe::kMaxKSplits) s = moe::kMaxKSplits;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+int64_t gemm_n_blocks(const moe_shape_t& s, int stage) { return stage == 1 ? s.I / 128 : (s.K + 255) / 256; }
+int64_t gemm_k_blocks(const moe_shape_t& s, int stage, bool fp8) { return (stage == 1 ? s.K : s.I) / (fp8 ? 128 : 64); }
+
 void compute_ws_layout(moe_ctx* c) {
   const moe_shape_t& s = c->shape;
   moe_ws_layout_t& w = c->ws;
@@ -201,6 +220,17 @@ void compute_ws_layout(moe_ctx* c) {
   w.h = take(static_cast<uint64_t>(w.rows) * s.I * esize);
   w.h_sf = take(c->fp8 ? static_cast<uint64_t>(w.blocks) * (s.I / 128) * 512 : 0);
   w.y = take(static_cast<uint64_t>(w.rows) * s.K * 2);
+  // masked layout: split-K tables and partial sums (see moe_ws_layout_t)
+  const bool masked = c->layout == MOE_LAYOUT_MASKED;
+  const int64_t nb1 = gemm_n_blocks(s, 1), nb2 = gemm_n_blocks(s, 2);
+  w.k_splits1 = masked ? k_splits_for(nb1, gemm_k_blocks(s, 1, c->fp8)) : 1;
+  w.k_splits2 = masked ? k_splits_for(nb2, gemm_k_blocks(s, 2, c->fp8)) : 1;
+  const bool split = w.k_splits1 > 1 || w.k_splits2 > 1;
+  w.partial_rows = split ? (A < w.rows ? A : w.rows) : 0;
+  const uint64_t p1 = static_cast<uint64_t>(w.k_splits1 > 1 ? w.k_splits1 : 0) * nb1 * 256;
+  const uint64_t p2 = static_cast<uint64_t>(w.k_splits2 > 1 ? w.k_splits2 : 0) * nb2 * 256;
+  w.block_vrow = take(split ? 4 * static_cast<uint64_t>(w.blocks) : 0);
+  w.partial = take(4 * static_cast<uint64_t>(w.partial_rows) * (p1 > p2 ? p1 : p2));
   w.total_bytes = off;
 }
 
@@ -248,11 +278,18 @@ moe::GemmArgs gemm_args(const moe_ctx* c, void* ws, int stage) {
   g.fp4 = c->fp4;
   g.masked = c->layout == MOE_LAYOUT_MASKED;
   g.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
-  const int64_t red = stage == 1 ? s.K : s.I;
-  g.k_blocks = static_cast<int32_t>(red / (c->fp8 ? 128 : 64));
+  g.k_blocks = static_cast<int32_t>(gemm_k_blocks(s, stage, c->fp8));
   g.timeout_ns = c->timeout_ns;
+  g.max_m = static_cast<int32_t>(s.max_m);
+  g.k_splits = stage == 1 ? c->ws.k_splits1 : c->ws.k_splits2;
+  if (g.k_splits > 1) {
+    g.block_vrow = at<int32_t>(ws, c->ws.block_vrow);
+    g.partial = at<float>(ws, c->ws.partial);
+    g.part_rows = c->ws.partial_rows;
+    g.part_cols = gemm_n_blocks(s, stage) * 256;
+  }
   if (stage == 1) {
-    g.n_blocks = static_cast<int32_t>(s.I / 128);
+    g.n_blocks = static_cast<int32_t>(gemm_n_blocks(s, 1));
     g.n_half = s.I;
     g.n_total = s.I;
     g.w_rows_blocks = static_cast<int32_t>(2 * s.I / 128);
@@ -264,7 +301,7 @@ moe::GemmArgs gemm_args(const moe_ctx* c, void* ws, int stage) {
     g.out_sf = at<uint8_t>(ws, c->ws.h_sf);
     g.out_groups = static_cast<int32_t>(s.I / 128);
   } else {
-    g.n_blocks = static_cast<int32_t>((s.K + 255) / 256);
+    g.n_blocks = static_cast<int32_t>(gemm_n_blocks(s, 2));
     g.n_half = 0;
     g.n_total = s.K;
     g.w_rows_blocks = static_cast<int32_t>(s.K / 128);
@@ -385,6 +422,7 @@ moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, vo
   p.block_info = at<int32_t>(ws, ctx->ws.block_info);
   p.chunk_hist = at<int32_t>(ws, ctx->ws.chunk_hist);
   p.chunk_rank = at<int32_t>(ws, ctx->ws.chunk_rank);
+  if (ctx->ws.partial_rows > 0) p.block_vrow = at<int32_t>(ws, ctx->ws.block_vrow);
   return cuda_status(moe::launch_plan(p, static_cast<cudaStream_t>(stream)));
 }
 
@@ -418,7 +456,7 @@ static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
   st = ensure_ws_maps(ctx, ws);
   if (st != MOE_OK) return st;
   const moe::GemmArgs g = gemm_args(ctx, ws, stage);
-  int64_t max_tiles = ctx->ws.blocks * g.n_blocks;
+  int64_t max_tiles = ctx->ws.blocks * g.n_blocks * g.k_splits;
   int grid = ctx->num_sms;
   if (max_tiles < grid) grid = static_cast<int>(max_tiles);
   moe::GemmMaps m;
@@ -426,7 +464,10 @@ static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
   m.b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
   m.out = stage == 1 ? ctx->map_a : ctx->map_y;   // stage 1 stores through plain writes
   m.wsf = ctx->mx ? (stage == 1 ? ctx->map_w13_sf : ctx->map_w2_sf) : m.b;   // (not read without MX scales)
-  return cuda_status(moe::launch_gemm(g, m, grid, static_cast<cudaStream_t>(stream)));
+  cudaError_t e = moe::launch_gemm(g, m, grid, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && g.k_splits > 1)
+    e = moe::launch_split_reduce(g, ctx->ws.blocks * g.n_blocks, static_cast<cudaStream_t>(stream));
+  return cuda_status(e);
 }
 
 moe_status_t moe_grouped_gemm_w13_act(moe_ctx* ctx, void* ws, void* stream) { return run_gemm(ctx, ws, stream, 1); }
@@ -465,7 +506,10 @@ int32_t moe_forward_launches(const moe_ctx* ctx) {
   const moe_shape_t& s = ctx->shape;
   int n = moe::plan_launch_count(s.T * s.topk, s.E_local);   // plan
   if (s.T > 0) n += 2;                          // quant + combine
-  if (ctx->ws.blocks > 0) n += 2;               // two GEMMs
+  if (ctx->ws.blocks > 0) {
+    n += 2;                                     // two GEMMs
+    n += (ctx->ws.k_splits1 > 1) + (ctx->ws.k_splits2 > 1);   // their split-K reductions
+  }
   return n;
 }
 

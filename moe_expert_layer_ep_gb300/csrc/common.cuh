@@ -245,6 +245,9 @@ __device__ __forceinline__ int ue8m0_exponent(float amax) {
   return s < -127 ? -127 : (s > 127 ? 127 : s);
 }
 
+// SiLU(gate) * up in fp32 (the fused activation of the first expert GEMM).
+__device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
+
 // 2^-s as fp32 for s in [-127, 126] (exact).
 __device__ __forceinline__ float exp2_neg(int s) { return __uint_as_float(static_cast<uint32_t>(127 - s) << 23); }
 

@@ -67,13 +67,17 @@ namespace {
 // two per accumulator lane quadrant with half of the columns each, copies the
 // accumulator out and releases it before the activation and quantisation.
 // The others use 4 warps (measured faster there).
-__host__ __device__ constexpr int epi_warps(bool fp8, int stage) { return (fp8 && stage == 1) ? 8 : 4; }
+// Split-K kernels (masked layouts) copy the accumulator out to the partial
+// buffer in 32-column chunks and use 4 warps.
+__host__ __device__ constexpr int epi_warps(bool fp8, int stage, bool split = false) {
+  return (fp8 && stage == 1 && !split) ? 8 : 4;
+}
 // FP8 with 128x128 weight scales: one warp expands each stage's weight-scale
 // tile in shared memory, beside the TMA producer (whose loop then only
 // issues copies).
 __host__ __device__ constexpr int scale_warps(bool fp8, bool mx) { return fp8 && !mx ? 1 : 0; }
-__host__ __device__ constexpr int threads_for(bool fp8, bool mx, int stage) {
-  return 64 + 32 * epi_warps(fp8, stage) + 32 * scale_warps(fp8, mx);
+__host__ __device__ constexpr int threads_for(bool fp8, bool mx, int stage, bool split) {
+  return 64 + 32 * epi_warps(fp8, stage, split) + 32 * scale_warps(fp8, mx);
 }
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
@@ -151,15 +155,16 @@ __device__ __forceinline__ void tile_b_rows(const GemmArgs& g, const Tile& tl, i
   }
 }
 
-__device__ __forceinline__ float silu_mul(float gate, float up) { return gate / (1.0f + __expf(-gate)) * up; }
+// First K block of segment seg when the K loop runs in S fixed segments.
+__device__ __forceinline__ int seg_begin(int seg, int S, int k_blocks) { return seg * k_blocks / S; }
 
 // Tensor maps: map_a (A rows), map_b (weights; GEMM1 as [E][gate, up][I/128]
 // [128 rows][K] so that one box holds a tile's gate and up rows, GEMM2 in
 // 256-row boxes), map_out (GEMM2 y stores), map_wsf (MXFP8 weight-scale
 // chunks, both of a tile's chunks in one box).
 // kFP4: MXFP4 weights, an E2M1 B operand (with kFP8 and kMX).
-template <bool kFP8, bool kMX, int kStage, bool kFP4>
-__global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
+template <bool kFP8, bool kMX, int kStage, bool kFP4, bool kSplit>
+__global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const __grid_constant__ CUtensorMap map_out, const __grid_constant__ CUtensorMap map_wsf,
                         const GemmArgs g) {
@@ -192,11 +197,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage));
+      mbar_init(&tempty[a], 32 * epi_warps(kFP8, kStage, kSplit));
     }
     mbar_init(done, 1);
     for (int q = 0; q < 4; ++q) mbar_init(&xchg[q], 64);
-    mbar_init(esync, 32 * epi_warps(kFP8, kStage));
+    mbar_init(esync, 32 * epi_warps(kFP8, kStage, kSplit));
     if (kStage == 2) prefetch_tensormap(&map_out);
     *abort_flag = 0;
     fence_barrier_init();
@@ -215,6 +220,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
 
   const int64_t n_tiles = static_cast<int64_t>(g.meta[1]) * g.n_blocks;
   const int k_blocks = g.k_blocks;
+  // work unit u: tile u / S, K segment u % S (S = 1 unless split)
+  const int S = kSplit ? g.k_splits : 1;
+  const int64_t n_units = n_tiles * S;
   constexpr int kElemsPerKBlock = kFP8 ? 128 : 64;
 
   if (warp == 0) {
@@ -224,12 +232,15 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
 
-    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int64_t t = u / S;
+      const int seg = static_cast<int>(u - t * S);
       const Tile tl = load_tile(g, t);
       int r0, r1;
       tile_b_rows<kStage>(g, tl, &r0, &r1);
       const int a_e = g.masked ? tl.expert : 0;
-      for (int kb = 0; kb < k_blocks; ++kb) {
+      const int kb_end = seg_begin(seg + 1, S, k_blocks);
+      for (int kb = seg_begin(seg, S, k_blocks); kb < kb_end; ++kb) {
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, g.timeout_ns);
         w_ok = __shfl_sync(0xFFFFFFFFu, w_ok, 0);
@@ -295,7 +306,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++iter) {
+      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++iter) {
+        const int seg = static_cast<int>(u % S);
         const int acc = kFP8 ? 0 : (iter & 1);
         const uint32_t acc_phase = kFP8 ? (iter & 1) : ((iter >> 1) & 1);
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1, abort_flag, g.timeout_ns)) {
@@ -304,7 +316,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kTileN);
-        for (int kb = 0; kb < k_blocks; ++kb) {
+        const int kb_begin = seg_begin(seg, S, k_blocks), kb_end = seg_begin(seg + 1, S, k_blocks);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          const uint32_t first = kb == kb_begin;   // the segment's first K block starts the sum
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, g.timeout_ns)) {
             ok = false;
             break;
@@ -327,10 +341,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
               mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
                                    kMX ? (kIdescB | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4))
                                        : kIdescB,
-                                   sfa_t, sfb_t, (kb | k) != 0);
+                                   sfa_t, sfb_t, !(first && k == 0));
           } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescBF16, (kb | k) != 0);
+            for (int k = 0; k < 4; ++k)
+              mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescBF16, !(first && k == 0));
           }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -350,7 +365,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
       const int never = 0;
       mbar_wait_bounded(done, 0, &never, g.timeout_ns);
     }
-  } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage)) {
+  } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage, kSplit)) {
     // ------------------------------------------------------------------ weight-scale tiles (FP8)
     // B scale tile of each stage: 256 rows, rows 0..127 share the first
     // weight block's scale, rows 128..255 the second's; 1 KB written by the
@@ -358,7 +373,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int64_t t = u / S;
+      const int seg = static_cast<int>(u - t * S);
       const Tile tl = load_tile(g, t);
       int r0, r1;
       tile_b_rows<kStage>(g, tl, &r0, &r1);
@@ -366,11 +383,12 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
       const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
       const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
       uint32_t sg_cache = 0, su_cache = 0;
-      for (int kb = 0; kb < k_blocks; ++kb) {
-        if ((kb & 31) == 0) {
+      const int kb_begin = seg_begin(seg, S, k_blocks), kb_end = seg_begin(seg + 1, S, k_blocks);
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (((kb - kb_begin) & 31) == 0) {
           // weight scales of the next 32 K blocks, one per lane
           const int kk = kb + lane;
-          if (kk < k_blocks) {
+          if (kk < kb_end) {
             sg_cache = g.w_sf[(base + b0) * g.w_k_groups + kk];
             su_cache = g.w_sf[(base + b1) * g.w_k_groups + kk];
           }
@@ -382,8 +400,8 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
           ok = false;
           break;
         }
-        const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, kb & 31);
-        const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, kb & 31);
+        const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, (kb - kb_begin) & 31);
+        const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, (kb - kb_begin) & 31);
         const uint32_t word = (lane < 16 ? sg : su) * 0x01010101u;
         uint4* dst = reinterpret_cast<uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane * 2;
         dst[0] = make_uint4(word, word, word, word);
@@ -407,14 +425,15 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
     // owning half of the tile's columns.  A thread copies its accumulator
     // slice to registers and releases the accumulator before any math, so
     // the next tile's MMAs never wait on activation, quantisation or stores.
-    constexpr int kEpiWarps = epi_warps(kFP8, kStage);
+    constexpr int kEpiWarps = epi_warps(kFP8, kStage, kSplit);
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;  // 0 when there are four epilogue warps
     const int r = quad * 32 + lane;
     float* s_amax = reinterpret_cast<float*>(smem + kOffAmax);  // [2 parities][4 quads][2 halves][32]
     int iter = 0;
     uint32_t chunk_ctr = 0;   // GEMM2: staged chunks so far (staging tile and barrier parity)
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++iter) {
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++iter) {
+      const int64_t t = u / S;
       const Tile tl = load_tile(g, t);
       const int acc = kFP8 ? 0 : (iter & 1);
       const uint32_t acc_phase = kFP8 ? (iter & 1) : ((iter >> 1) & 1);
@@ -430,6 +449,44 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
       const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kTileN) + (static_cast<uint32_t>(quad * 32) << 16);
       const bool row_ok = r < tl.valid;
       const int64_t row = tl.row0 + r;
+      if constexpr (kSplit) {
+        // ---- split K: this segment's sums of the valid rows go to the
+        // partial buffer; the stage's reduce kernel, launched next, adds the
+        // segments in order and applies the epilogue.
+        const int seg = static_cast<int>(u - t * S);
+        const bool quad_rows = quad * 32 < tl.valid;     // warp-uniform
+        const int64_t vrow = g.block_vrow[t / g.n_blocks];
+        float* prow = g.partial + (static_cast<int64_t>(seg) * g.part_rows + vrow + r) * g.part_cols +
+                      static_cast<int64_t>(tl.nb) * 256;
+        if (!quad_rows) {
+          tc_fence_before();
+          mbar_arrive(&tempty[acc]);
+          continue;
+        }
+        {
+          // the warp's 32 rows, all 256 accumulator columns, 32 at a time
+          constexpr int kChunks = kTileN / 32;
+#pragma unroll 1
+          for (int c = 0; c < kChunks; ++c) {
+            const uint32_t col = static_cast<uint32_t>(32 * c);
+            uint32_t v32[32];
+            tmem_ld_32x32b_x32(taddr + col, v32);
+            tmem_ld_wait();
+            if (c == kChunks - 1) {
+              tc_fence_before();
+              mbar_arrive(&tempty[acc]);
+            }
+            if (row_ok) {
+              float4* d = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                d[v] = make_float4(__uint_as_float(v32[4 * v]), __uint_as_float(v32[4 * v + 1]),
+                                   __uint_as_float(v32[4 * v + 2]), __uint_as_float(v32[4 * v + 3]));
+            }
+          }
+        }
+        continue;
+      }
       if (kStage == 1 && kEpiWarps == 4) {
         uint16_t* dst = static_cast<uint16_t*>(g.out) + row * g.out_ld + tl.nb * 128;
 #pragma unroll 1
@@ -654,19 +711,33 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage), 1)
   }
 }
 
-template <bool kFP8, bool kMX, int kStage, bool kFP4 = false>
+template <bool kFP8, bool kMX, int kStage, bool kFP4, bool kSplit>
 cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
   constexpr int kSmemBytes = Lay::kSmemBytes;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4>
-      <<<grid, threads_for(kFP8, kMX, kStage), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
+  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>
+      <<<grid, threads_for(kFP8, kMX, kStage, kSplit), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
   return cudaGetLastError();
+}
+
+template <bool kFP8, bool kMX, bool kFP4, bool kSplit>
+cudaError_t launch_stage(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
+  return g.stage == 1 ? launch_one<kFP8, kMX, 1, kFP4, kSplit>(g, m, grid, s)
+                      : launch_one<kFP8, kMX, 2, kFP4, kSplit>(g, m, grid, s);
+}
+
+template <bool kSplit>
+cudaError_t launch_dtype(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
+  if (g.fp4) return launch_stage<true, true, true, kSplit>(g, m, grid, s);
+  if (g.mx) return launch_stage<true, true, false, kSplit>(g, m, grid, s);
+  if (g.fp8) return launch_stage<true, false, false, kSplit>(g, m, grid, s);
+  return launch_stage<false, false, false, kSplit>(g, m, grid, s);
 }
 
 __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
@@ -688,17 +759,7 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 
 
 cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
-  if (g.fp4)
-    return g.stage == 1 ? launch_one<true, true, 1, true>(g, m, grid, s) : launch_one<true, true, 2, true>(g, m, grid, s);
-  if (g.mx) {
-    return g.stage == 1 ? launch_one<true, true, 1>(g, m, grid, s) : launch_one<true, true, 2>(g, m, grid, s);
-  }
-  if (g.fp8) {
-    return g.stage == 1 ? launch_one<true, false, 1>(g, m, grid, s)
-                        : launch_one<true, false, 2>(g, m, grid, s);
-  }
-  return g.stage == 1 ? launch_one<false, false, 1>(g, m, grid, s)
-                      : launch_one<false, false, 2>(g, m, grid, s);
+  return g.k_splits > 1 ? launch_dtype<true>(g, m, grid, s) : launch_dtype<false>(g, m, grid, s);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {

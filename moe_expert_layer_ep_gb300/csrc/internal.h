@@ -13,6 +13,7 @@ constexpr int kMaxTopk = 64;
 constexpr int kBlockM = 128;      // rows per expert block == compact block_e
 constexpr int kMaxRouterExperts = 1024;
 constexpr int kRouterSegment = 1024;     // K elements per router partial sum (fixed, batch-independent)
+constexpr int kMaxKSplits = 8;           // K segments of a masked-layout GEMM tile, at most
 
 struct PlanArgs {
   const int32_t* topk_ids;  // [A]
@@ -34,6 +35,7 @@ struct PlanArgs {
   int32_t* block_info;      // int4 per block
   int32_t* chunk_hist;      // [E_local, chunks]
   int32_t* chunk_rank;      // [A]
+  int32_t* block_vrow;      // masked, optional: [blocks] first valid-row index of each block
 };
 
 struct QuantArgs {
@@ -83,6 +85,16 @@ struct GemmArgs {
   uint8_t* out_sf;            // stage 1 fp8: h scale chunks
   int32_t out_groups;         // stage 1 fp8: I / 128
   uint64_t timeout_ns;
+  // Split K (masked layouts): each tile's K loop runs in k_splits fixed
+  // segments; segment s writes the tile's valid rows' fp32 sums to
+  // partial[s][row][col] and launch_split_reduce then adds the segments in
+  // order and applies the stage's epilogue.
+  int32_t k_splits;           // 1: no split
+  int32_t max_m;              // masked rows per expert
+  const int32_t* block_vrow;  // [blocks] first valid-row index of each block
+  float* partial;             // [k_splits][part_rows][part_cols]
+  int64_t part_rows;
+  int64_t part_cols;          // n_blocks * 256
 };
 
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
@@ -98,6 +110,10 @@ struct GemmMaps {
   CUtensorMap wsf;   // MXFP8 / MXFP4: packed weight-scale chunks, a tile's two chunks per box
 };
 cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& maps, int grid, cudaStream_t s);
+// After a split-K GEMM launch: adds each valid row's segment sums in segment
+// order and writes h (stage 1: SiLU*up, then FP8 / MXFP8 / bf16 storage) or y
+// (stage 2: bf16).  max_tiles: the static bound on the launch's tiles.
+cudaError_t launch_split_reduce(const GemmArgs& g, int64_t max_tiles, cudaStream_t s);
 cudaError_t launch_requant(const uint8_t* w_in, const float* s_in, uint8_t* w_out, uint8_t* s_out, int64_t E,
                            int64_t N, int64_t C, cudaStream_t s);
 cudaError_t launch_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst, int64_t E, int64_t N, int64_t C,

@@ -133,6 +133,9 @@ __device__ void expert_tables(const PlanArgs& p, const int* s_count, int* s_warp
         info.z = b * kBlockM;
         const int left = rows - b * kBlockM;
         info.w = left < kBlockM ? left : kBlockM;
+        // valid rows numbered without padding: expert e's rows start at the
+        // sum of the earlier experts' valid rows
+        if (p.block_vrow) p.block_vrow[blk_start + b] = row_start + b * kBlockM;
       }
       reinterpret_cast<int4*>(p.block_info)[blk_start + b] = info;
     }

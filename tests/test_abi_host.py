@@ -64,3 +64,23 @@ def test_noalloc_plan_rejects_masked_row_offsets_beyond_int32():
     shape.max_m = (1 << 26) - 1                                 # fits: the next check (null outputs) answers
     code = M._lib.moe_plan_layout_noalloc(ctypes.byref(shape), None, ctypes.byref(outs), None)
     assert code == M.STATUS["MOE_ERR_INVALID_ARG"]
+
+
+def test_workspace_layout_struct_matches_the_header():
+    """The binding's mirror of moe_ws_layout_t has the C struct's size and
+    field offsets (a shorter mirror would let the library write past it)."""
+    import ctypes
+    text = open(HEADER).read()
+    body = text[text.index("typedef struct {\n  uint64_t total_bytes;"):text.index("} moe_ws_layout_t;")]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"(u?int(?:32|64)_t)\s+(\w+);", body)
+    names = [n for _, n in fields]
+    assert names == [f[0] for f in M.MoeWsLayout._fields_]
+    size = {"uint64_t": 8, "int64_t": 8, "int32_t": 4}
+    off = 0
+    for (ty, name) in fields:
+        a = size[ty]
+        off = (off + a - 1) // a * a
+        assert getattr(M.MoeWsLayout, name).offset == off, name
+        off += a
+    assert ctypes.sizeof(M.MoeWsLayout) == (off + 7) // 8 * 8

@@ -42,6 +42,14 @@ CASES = [
     dict(T=48, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp4", layout="masked", expert_start=16),
     dict(T=300, K=640, I=384, E_global=12, E_local=12, topk=4, dtype="mxfp8", layout="compact", drop_every=5),
     dict(T=200, K=384, I=256, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
+    # masked layouts whose GEMMs run in K segments (GEMM1 4 or 8, GEMM2 2 or 4
+    # segments), one of them ragged (5 K blocks in segments of 2 and 3), and
+    # experts with rows in two blocks and in several lane quadrants
+    dict(T=48, K=1024, I=512, E_global=64, E_local=16, topk=8, dtype="fp8", layout="masked", expert_start=16),
+    dict(T=48, K=1024, I=512, E_global=64, E_local=16, topk=8, dtype="bf16", layout="masked", expert_start=16),
+    dict(T=100, K=1024, I=512, E_global=64, E_local=16, topk=8, dtype="mxfp8", layout="masked", expert_start=16),
+    dict(T=40, K=1024, I=512, E_global=64, E_local=16, topk=8, dtype="mxfp4", layout="masked", expert_start=16),
+    dict(T=700, K=640, I=384, E_global=16, E_local=4, topk=4, dtype="fp8", layout="masked", expert_start=4),
 ]
 
 
@@ -106,7 +114,10 @@ def test_gemm2_matches_oracle(case):
     assert err <= 2e-3, err
 
 
-@pytest.mark.parametrize("case", CASES[:4], ids=[_ids(c) for c in CASES[:4]])
+COMBINE_CASES = CASES[:6] + CASES[-2:]     # compact and masked, split and unsplit GEMMs
+
+
+@pytest.mark.parametrize("case", COMBINE_CASES, ids=[_ids(c) for c in COMBINE_CASES])
 def test_combine_matches_oracle(case):
     p = Problem(**case)
     g = p.gpu()
@@ -131,14 +142,15 @@ def test_combine_matches_oracle(case):
     assert rel_fro(got, ref) <= 1e-3
 
 
-@pytest.mark.parametrize("layout", ["compact", "masked"])
-def test_gemm2_block_scales_exact(layout):
+@pytest.mark.parametrize("layout,I", [("compact", 256), ("masked", 256), ("masked", 512)])
+def test_gemm2_block_scales_exact(layout, I):
     """FP8 GEMM2 with every h and w2 element 1.0 (E4M3 0x38): row r of a
     128-row block gets scale 2^(r-64) and weight row block b gets 2^(b%3-1),
     so y[r, n] = I * 2^(r - 64 + b%3 - 1) exactly.  A wrong scale placement
-    shows up as the row whose scale was used."""
+    shows up as the row whose scale was used.  With I = 512 the masked GEMM2
+    runs its K loop in two segments, whose exact sums must add up exactly."""
     import moe_expert_layer_ep_gb300 as M
-    T, K, I, E = 256, 384, 256, 2
+    T, K, E = 256, 384, 2
     kw = dict(T=T, K=K, I=I, E_global=E if layout == "compact" else 4, E_local=E, topk=1, dtype="fp8",
               layout=layout, weight_device="cpu")
     p = Problem(**kw)
@@ -180,3 +192,50 @@ def test_gemm2_block_scales_exact(layout):
         pytest.fail(f"scale placement wrong: row-in-block -> scale row used: "
                     f"{[(int(r_in[i]), float(used[i])) for i in bad]}; col mismatches "
                     f"{np.count_nonzero(y != expect)} of {y.size}")
+
+
+@pytest.mark.parametrize("layout", ["compact", "masked"])
+def test_gemm_stages_full_size_experts(layout):
+    """GEMM1 and GEMM2 at the large-prefill shape (K=7168, I=2048, FP8 with
+    128x128 weight scales) on every valid row of three experts, each stage fed
+    the CUDA path's own input.  Compact: 256 experts with Zipf routing; the
+    experts checked are the most used one (several 128-row blocks), the
+    highest-numbered one with rows (index above 73: its w13 offset passes 2^31
+    elements) and one whose only block is partial.  Masked: 32 local experts
+    of 256 at T=256, where the w13 GEMM runs its K loop in segments."""
+    import synth
+    w = synth.WORKLOADS["fp8_prefill_zipf"]
+    if layout == "compact":
+        p = Problem(T=1024, K=w["K"], I=w["I"], E_global=256, E_local=256, topk=8, dtype="fp8", layout="compact",
+                    seed=w["seed"], zipf_s=w["zipf_s"])
+    else:
+        p = Problem(T=256, K=w["K"], I=w["I"], E_global=256, E_local=32, topk=8, dtype="fp8", layout="masked",
+                    max_m=256, seed=w["seed"] + 5, weight_seed=w["seed"] + 2)
+    g = p.gpu()
+    g.plan(); g.quant(); g.gemm1(); g.gemm2()
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    o = p.oracle_plan()
+    counts = o["counts"]
+    nz = np.flatnonzero(counts)
+    big = int(nz[np.argmax(counts[nz])])
+    high = int(nz.max())
+    part = int(next(e for e in nz[np.argsort(counts[nz])] if e not in (big, high)))
+    if layout == "compact":
+        assert counts[big] > 256 and high > 73 and counts[part] < 128
+    else:
+        assert g.ctx.ws_layout.k_splits1 > 1 and g.ctx.ws_layout.k_splits2 == 1
+    for e in (big, high, part):
+        if layout == "compact":
+            rows = np.flatnonzero(o["m_indices"] == e)
+        else:
+            rows = e * p.max_m + np.arange(o["masked_m"][e])
+        w13, w2 = p.expert_weights64(e)
+        a = g.decoded("a", rows)
+        h_gpu = g.decoded("h", rows)
+        _, _, h = oracle.gemm1_act(a, w13)
+        h_ref, _ = oracle.store_act(h, "fp8")
+        assert rel_fro(h_gpu, h_ref) <= 2e-3, (e, "gemm1")
+        assert np.mean(h_gpu != h_ref) <= 5e-3, (e, "gemm1 flips")
+        y_gpu = bf16_to_f64(g.view("y").index_select(0, torch.as_tensor(rows, device="cuda")))
+        assert rel_fro(y_gpu, oracle.gemm2(h_gpu, w2)) <= 2e-3, (e, "gemm2")

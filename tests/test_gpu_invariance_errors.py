@@ -94,6 +94,71 @@ def test_batch_invariance_sweep(dtype, request):
             assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (T, rep)
 
 
+E_LOCAL_DECODE = 32
+
+
+def _run_masked(dtype, weights, x, ids, w, max_m):
+    """The layer for a rank holding experts 0..31 of 256 (masked layout)."""
+    T, EL = x.shape[0], E_LOCAL_DECODE
+    shape = M.make_shape(T, K, I, E, EL, TOPK, dtype, "masked", 0, max_m)
+    if dtype in ("fp8", "mxfp8", "mxfp4"):
+        ctx = M.moe_ctx_create(shape, weights[0][:EL], weights[1][:EL], weights[2][:EL], weights[3][:EL])
+    else:
+        ctx = M.moe_ctx_create(shape, weights[0][:EL], None, weights[1][:EL], None)
+    ws = M.alloc_workspace(ctx)
+    out = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+    M.moe_forward(ctx, x, ids, w, ws, out)
+    torch.cuda.synchronize()
+    assert M.moe_read_device_status(ws) == 0
+    return out, ctx.ws_layout
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "mxfp8", "mxfp4", "bf16"])
+def test_masked_decode_batch_invariance(dtype, request):
+    """The masked (expert-parallel decode) layout splits each GEMM tile's K
+    loop into segments fixed by K and I alone; a token's output bits must
+    still not depend on the batch size, its position or max_m.  Probe tokens
+    that route to at least one local expert are placed among filler tokens
+    for T = 1, 16, 64 and 256 (max_m = T rounded up to 16), twice each."""
+    weights = request.getfixturevalue({"fp8": "weights_fp8", "mxfp8": "weights_mx", "mxfp4": "weights_mx4",
+                                       "bf16": "weights_bf16"}[dtype])
+    px, pids, pw = synth.probe_tokens(16, K, E, TOPK, SEED + 17)
+    local = ((pids >= 0) & (pids < E_LOCAL_DECODE)).any(dim=1).numpy()
+    keep = np.flatnonzero(local)[:3]
+    assert keep.size == 3
+    px, pids, pw = px[keep], pids[keep].contiguous(), pw[keep].contiguous()
+    ref = None
+    rng = np.random.default_rng(9)
+    splits = None
+    for T in (1, 16, 64, 256):
+        max_m = (T + 15) // 16 * 16
+        for rep in range(2):
+            if T == 1:
+                rows = []
+                for i in range(3):
+                    out, L = _run_masked(dtype, weights, px[i:i + 1].cuda(), pids[i:i + 1].cuda(),
+                                         pw[i:i + 1].cuda(), max_m)
+                    rows.append(out[0].clone())
+                got = torch.stack(rows)
+            else:
+                fx = synth.activations(T, K, 3000 + T + rep, "cuda")
+                fids, fw = synth.routing(T, E, TOPK, 4000 + T + rep)
+                pos = rng.choice(T, size=3, replace=False)
+                fx[pos] = px.cuda()
+                fids[pos] = pids
+                fw[pos] = pw
+                out, L = _run_masked(dtype, weights, fx, fids.cuda(), fw.cuda(), max_m)
+                got = out[torch.as_tensor(pos, device="cuda")].clone()
+            if ref is None:
+                ref = got
+            assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (T, rep)
+            # the split is the same at every T (it depends on K and I only)
+            assert splits in (None, (L.k_splits1, L.k_splits2))
+            splits = (L.k_splits1, L.k_splits2)
+    assert splits[0] > 1 and splits[1] == 1      # K=7168, I=2048: w13 in segments, w2 whole
+    assert ref.abs().max() > 0
+
+
 def test_bad_expert_id_sets_status_and_is_dropped():
     p = Problem(T=64, K=256, I=128, E_global=8, E_local=8, topk=2, dtype="fp8", layout="compact",
                 weight_device="cpu")
