@@ -151,16 +151,19 @@ def kernel_source_digest():
     return "-".join(parts)
 
 
-def measured_traffic(workload_name):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when the kernel code changed since the capture."""
+def measured_traffic(workload_name, T_override=None, key="dram_bytes_per_launch"):
+    """DRAM bytes per launch of a GEMM kernel (the dominant one, or GEMM2 with
+    key="gemm2_dram_bytes_per_launch") from the committed ncu summary of this
+    workload (and token count, when overridden), or None when there is no
+    capture or the kernel code changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    rec = json.load(open(path)).get(workload_name)
-    if not rec:
+    name = workload_name if T_override is None else f"{workload_name}@T{T_override}"
+    rec = json.load(open(path)).get(name)
+    if not rec or key not in rec:
         return None
-    return rec["dram_bytes_per_launch"] if kernel_source_digest() == rec["code_digest"] else None
+    return rec[key] if kernel_source_digest() == rec["code_digest"] else None
 
 
 def workload(args):
@@ -578,8 +581,9 @@ def run_ours(args, w, world, rank, local):
     exec1 = 2.0 * padded_rows * w["K"] * 2 * w["I"] / (g1_ms / 1000.0) / 1e12
     exec2 = 2.0 * padded_rows * w["I"] * w["K"] / (g2_ms / 1000.0) / 1e12
     roof.update({"executed_tflops": round(exec1, 1), "executed_tensor_frac": round(exec1 / tensor_peak, 4),
-                 "traffic": measured_traffic(w["name"]) if not args.T else None})
-    roof2.update({"executed_tflops": round(exec2, 1), "executed_tensor_frac": round(exec2 / tensor_peak, 4)})
+                 "traffic": measured_traffic(w["name"], args.T)})
+    roof2.update({"executed_tflops": round(exec2, 1), "executed_tensor_frac": round(exec2 / tensor_peak, 4),
+                  "traffic": measured_traffic(w["name"], args.T, "gemm2_dram_bytes_per_launch")})
     layer_roof_ms = 1000.0 * max(wm["layer_bytes"] / (peaks["hbm_gbs"] * 1e9),
                                  (wm["flops1"] + wm["flops2"]) / (tensor_peak * 1e12))
     fused_ms = 1000.0 * max(wm["fused_bytes"] / (peaks["hbm_gbs"] * 1e9),

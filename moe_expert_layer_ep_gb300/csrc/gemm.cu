@@ -218,12 +218,37 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
   tc_fence_after();
   const uint32_t tmem = *holder;
 
-  const int64_t n_tiles = static_cast<int64_t>(g.meta[1]) * g.n_blocks;
+  constexpr int kElemsPerKBlock = kFP8 ? 128 : 64;
   const int k_blocks = g.k_blocks;
   // work unit u: tile u / S, K segment u % S (S = 1 unless split)
   const int S = kSplit ? g.k_splits : 1;
+  if (warp == 0 && lane == 0) {
+    // While the previous kernel finishes, bring the first K blocks of this
+    // CTA's first weight tile into L2.  Inside the layer the block table was
+    // written two kernels back (by the plan), so it is complete here; were it
+    // not, a stale entry would only prefetch other weights (a prefetch reads
+    // nothing back and ignores coordinates outside the tensor).
+    const int64_t pre_units = static_cast<int64_t>(g.meta[1]) * g.n_blocks * S;
+    if (blockIdx.x < pre_units) {
+      const int64_t t = blockIdx.x / S;
+      const int seg = static_cast<int>(blockIdx.x - t * S);
+      const Tile tl = load_tile(g, t);
+      int r0, r1;
+      tile_b_rows<kStage>(g, tl, &r0, &r1);
+      const int kb0 = seg_begin(seg, S, k_blocks);
+      const int kb1 = min(seg_begin(seg + 1, S, k_blocks), kb0 + 8);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (kStage == 1)
+          tma_prefetch_5d(&map_b, kb * kElemsPerKBlock, 0, tl.nb, 0, tl.expert);
+        else
+          tma_prefetch_3d(&map_b, kb * kElemsPerKBlock, r0, tl.expert);
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  const int64_t n_tiles = static_cast<int64_t>(g.meta[1]) * g.n_blocks;
   const int64_t n_units = n_tiles * S;
-  constexpr int kElemsPerKBlock = kFP8 ? 128 : 64;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -721,9 +746,8 @@ cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStrea
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>
-      <<<grid, threads_for(kFP8, kMX, kStage, kSplit), kSmemBytes, s>>>(m.a, m.b, m.out, m.wsf, g);
-  return cudaGetLastError();
+  return launch_pdl(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>, dim3(grid),
+                    dim3(threads_for(kFP8, kMX, kStage, kSplit)), kSmemBytes, s, m.a, m.b, m.out, m.wsf, g);
 }
 
 template <bool kFP8, bool kMX, bool kFP4, bool kSplit>

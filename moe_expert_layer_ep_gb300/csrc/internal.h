@@ -5,7 +5,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace moe {
+
+// Launch a layer kernel with programmatic dependent launch allowed (it may
+// start while the stream's previous kernel runs; see pdl_wait in
+// common.cuh).  Inside a stream capture this becomes a programmatic edge of
+// the graph.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kPlanChunk = 256;   // assignments per plan CTA (8 warps x 32)
 constexpr int kMaxLocalExperts = 1024;
@@ -36,6 +58,7 @@ struct PlanArgs {
   int32_t* chunk_hist;      // [E_local, chunks]
   int32_t* chunk_rank;      // [A]
   int32_t* block_vrow;      // masked, optional: [blocks] first valid-row index of each block
+  int32_t clear_status;     // the one-CTA plan clears the status word itself (no memset launch)
 };
 
 struct QuantArgs {

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kPlanChunk) plan_count_rank(PlanArgs p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E_local;
   for (int i = tid; i < 8 * E; i += kPlanChunk) s_wcnt[i] = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   const int64_t i = static_cast<int64_t>(blockIdx.x) * kPlanChunk + tid;
@@ -150,6 +152,8 @@ __global__ void __launch_bounds__(1024) plan_scan(PlanArgs p) {
   __shared__ int s_warp[32];
   __shared__ int s_count[kMaxLocalExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
   // Warp w scans experts w, w + 32, w + 64, w + 96 (then the next four
   // groups): the exclusive scan of an expert's chunk counts becomes each
   // chunk's offset inside the expert, and its total the expert's count.
@@ -228,6 +232,8 @@ __device__ void fill_m_indices(const PlanArgs& p, const int32_t* s_tab, int64_t 
 __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
   extern __shared__ int32_t s_tab[];  // start[E], padded[E], counts[E] (compact)
   const int E = p.E_local;
+  pdl_wait();
+  pdl_trigger();
   if (!p.masked) {
     for (int x = threadIdx.x; x < E; x += blockDim.x) {
       s_tab[x] = p.start[x];
@@ -269,6 +275,11 @@ __global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E_local;
+  pdl_wait();
+  pdl_trigger();
+  // the status word reports the first data error of this pass
+  if (p.clear_status && tid < 4) p.status[tid] = 0;
+  __syncthreads();
   int* s_count = s_tab + 2 * E;
   for (int x = tid; x < E; x += 1024) s_count[x] = 0;
   int my_e[2] = {-1, -1};
@@ -334,23 +345,25 @@ int plan_launch_count(int64_t A, int32_t E_local) {
 }
 
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s) {
+  if (plan_is_small(p.A, p.E_local)) {
+    PlanArgs q = p;
+    q.clear_status = 1;   // the one CTA clears the status word before anything can set it
+    return launch_pdl(plan_small, dim3(1), dim3(1024), 0, s, q);
+  }
   // the status word reports the first data error of this pass through the layer
   cudaError_t e = cudaMemsetAsync(p.status, 0, 16, s);
   if (e != cudaSuccess) return e;
-  if (plan_is_small(p.A, p.E_local)) {
-    plan_small<<<1, 1024, 0, s>>>(p);
-    return cudaGetLastError();
-  }
   if (p.chunks > 0) {
-    plan_count_rank<<<p.chunks, kPlanChunk, 8 * p.E_local * sizeof(int32_t), s>>>(p);
+    e = launch_pdl(plan_count_rank, dim3(p.chunks), dim3(kPlanChunk), 8 * p.E_local * sizeof(int32_t), s, p);
+    if (e != cudaSuccess) return e;
   }
-  plan_scan<<<1, 1024, 0, s>>>(p);
+  e = launch_pdl(plan_scan, dim3(1), dim3(1024), 0, s, p);
+  if (e != cudaSuccess) return e;
   const int64_t work = p.A > p.all_tokens ? p.A : p.all_tokens;
   int grid = static_cast<int>((work + 255) / 256);
   if (grid > 1184) grid = 1184;
   if (grid < 1) grid = 1;
-  plan_finalize<<<grid, 256, 3 * p.E_local * sizeof(int32_t), s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(plan_finalize, dim3(grid), dim3(256), 3 * p.E_local * sizeof(int32_t), s, p);
 }
 
 }  // namespace moe

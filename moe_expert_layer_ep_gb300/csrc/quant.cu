@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs 
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x;
   if (tid == 0) s_any = 0;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   if (tid < q.topk) {
     const int64_t d = q.src2dst[t * q.topk + tid];
@@ -127,6 +129,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs c)
   __shared__ float s_w[kMaxTopk];
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (tid < c.topk) {
     s_dst[tid] = c.src2dst[t * c.topk + tid];
     s_w[tid] = c.topk_weights[t * c.topk + tid];
@@ -178,19 +182,15 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs c)
 
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s) {
   if (q.T <= 0) return cudaSuccess;
-  if (q.mx)
-    quant_scatter_kernel<true, true><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
-  else if (q.fp8)
-    quant_scatter_kernel<true, false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
-  else
-    quant_scatter_kernel<false, false><<<static_cast<unsigned>(q.T), kQuantThreads, 0, s>>>(q);
-  return cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(q.T)), block(kQuantThreads);
+  if (q.mx) return launch_pdl(quant_scatter_kernel<true, true>, grid, block, 0, s, q);
+  if (q.fp8) return launch_pdl(quant_scatter_kernel<true, false>, grid, block, 0, s, q);
+  return launch_pdl(quant_scatter_kernel<false, false>, grid, block, 0, s, q);
 }
 
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s) {
   if (c.T <= 0) return cudaSuccess;
-  combine_kernel<<<static_cast<unsigned>(c.T), kCombineThreads, 0, s>>>(c);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(static_cast<unsigned>(c.T)), dim3(kCombineThreads), 0, s, c);
 }
 
 }  // namespace moe

@@ -35,6 +35,8 @@ template <bool kFP8, bool kMX>
 __global__ void __launch_bounds__(kRedThreads) split_reduce_act_kernel(const GemmArgs g) {
   __shared__ float s_amax[2][4];
   const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
+  pdl_wait();
+  pdl_trigger();
   const int S = g.k_splits;
   const int64_t plane = g.part_rows * g.part_cols;
   const int64_t n_items = static_cast<int64_t>(g.meta[1]) * g.n_blocks;
@@ -93,6 +95,8 @@ __global__ void __launch_bounds__(kRedThreads) split_reduce_act_kernel(const Gem
 
 __global__ void __launch_bounds__(kRedThreads) split_reduce_y_kernel(const GemmArgs g) {
   const int c = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const int S = g.k_splits;
   const int64_t plane = g.part_rows * g.part_cols;
   const int64_t n_items = static_cast<int64_t>(g.meta[1]) * g.n_blocks;
@@ -127,16 +131,11 @@ __global__ void __launch_bounds__(kRedThreads) split_reduce_y_kernel(const GemmA
 cudaError_t launch_split_reduce(const GemmArgs& g, int64_t max_tiles, cudaStream_t s) {
   if (max_tiles <= 0) return cudaSuccess;
   const int grid = static_cast<int>(max_tiles < 1216 ? max_tiles : 1216);
-  if (g.stage == 2) {
-    split_reduce_y_kernel<<<grid, kRedThreads, 0, s>>>(g);
-  } else if (g.mx) {
-    split_reduce_act_kernel<true, true><<<grid, kRedThreads, 0, s>>>(g);
-  } else if (g.fp8) {
-    split_reduce_act_kernel<true, false><<<grid, kRedThreads, 0, s>>>(g);
-  } else {
-    split_reduce_act_kernel<false, false><<<grid, kRedThreads, 0, s>>>(g);
-  }
-  return cudaGetLastError();
+  const dim3 block(kRedThreads);
+  if (g.stage == 2) return launch_pdl(split_reduce_y_kernel, dim3(grid), block, 0, s, g);
+  if (g.mx) return launch_pdl(split_reduce_act_kernel<true, true>, dim3(grid), block, 0, s, g);
+  if (g.fp8) return launch_pdl(split_reduce_act_kernel<true, false>, dim3(grid), block, 0, s, g);
+  return launch_pdl(split_reduce_act_kernel<false, false>, dim3(grid), block, 0, s, g);
 }
 
 }  // namespace moe
