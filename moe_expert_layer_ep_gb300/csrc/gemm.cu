@@ -257,10 +257,15 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
     uint32_t issued_mask = 0, issued_parity = 0;
     bool ok = true;
 
+    // the next unit's block-table entry is read while the current unit's
+    // copies are issued, so no tile starts with a wait for it
+    Tile tl_next;
+    if (blockIdx.x < n_units) tl_next = load_tile(g, blockIdx.x / S);
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const int64_t t = u / S;
       const int seg = static_cast<int>(u - t * S);
-      const Tile tl = load_tile(g, t);
+      const Tile tl = tl_next;
+      if (u + gridDim.x < n_units) tl_next = load_tile(g, (u + gridDim.x) / S);
       int r0, r1;
       tile_b_rows<kStage>(g, tl, &r0, &r1);
       const int a_e = g.masked ? tl.expert : 0;
@@ -398,24 +403,41 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    // weight-scale rows of a unit's two weight row blocks, and the scales
+    // of its first 32 K blocks (one per lane); the next unit's are read
+    // while the current unit's tiles are written
+    auto unit_scales = [&](int64_t u, int64_t* base_sg, int64_t* base_su, uint32_t* sg, uint32_t* su) {
       const int64_t t = u / S;
       const int seg = static_cast<int>(u - t * S);
       const Tile tl = load_tile(g, t);
       int r0, r1;
       tile_b_rows<kStage>(g, tl, &r0, &r1);
-      const int b0 = min(r0 >> 7, g.w_rows_blocks - 1);
-      const int b1 = min(r1 >> 7, g.w_rows_blocks - 1);
       const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
-      uint32_t sg_cache = 0, su_cache = 0;
+      *base_sg = (base + min(r0 >> 7, g.w_rows_blocks - 1)) * g.w_k_groups;
+      *base_su = (base + min(r1 >> 7, g.w_rows_blocks - 1)) * g.w_k_groups;
+      const int kk = seg_begin(seg, S, k_blocks) + lane;
+      if (kk < seg_begin(seg + 1, S, k_blocks)) {
+        *sg = g.w_sf[*base_sg + kk];
+        *su = g.w_sf[*base_su + kk];
+      }
+    };
+    int64_t nb_sg = 0, nb_su = 0;
+    uint32_t n_sg = 0, n_su = 0;
+    if (blockIdx.x < n_units) unit_scales(blockIdx.x, &nb_sg, &nb_su, &n_sg, &n_su);
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const int64_t t = u / S;
+      const int seg = static_cast<int>(u - t * S);
+      const int64_t base_sg = nb_sg, base_su = nb_su;
+      uint32_t sg_cache = n_sg, su_cache = n_su;
+      if (u + gridDim.x < n_units) unit_scales(u + gridDim.x, &nb_sg, &nb_su, &n_sg, &n_su);
       const int kb_begin = seg_begin(seg, S, k_blocks), kb_end = seg_begin(seg + 1, S, k_blocks);
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (((kb - kb_begin) & 31) == 0) {
+        if (kb > kb_begin && ((kb - kb_begin) & 31) == 0) {
           // weight scales of the next 32 K blocks, one per lane
           const int kk = kb + lane;
           if (kk < kb_end) {
-            sg_cache = g.w_sf[(base + b0) * g.w_k_groups + kk];
-            su_cache = g.w_sf[(base + b1) * g.w_k_groups + kk];
+            sg_cache = g.w_sf[base_sg + kk];
+            su_cache = g.w_sf[base_su + kk];
           }
         }
         int w_ok = 1;

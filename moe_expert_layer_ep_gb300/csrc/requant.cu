@@ -13,7 +13,10 @@
 //   q' = e4m3(v * 2^-e)                    (round to nearest even, saturating)
 // One CTA per block: 512 threads, 32 bytes (a quarter row) each, read once,
 // reduced, written once; in-place operation (w_out == w_in) is allowed
-// because a CTA reads its whole block before writing it.
+// because a CTA reads its whole block before writing it.  A thread keeps only
+// its 32 raw e4m3 bytes in registers and forms the bf16 intermediate twice
+// (for the block maximum, then for the output), the same arithmetic both
+// times: with few registers per thread, three blocks are in flight per SM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,7 +31,7 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return __half2float(__half(hr));
 }
 
-__global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t* w_in, const float* s_in,
+__global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8_t* w_in, const float* s_in,
                                                                  uint8_t* w_out, uint8_t* s_out, int64_t N,
                                                                  int64_t C) {
   __shared__ float s_red[kRequantThreads / 32];
@@ -42,25 +45,26 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   const int64_t row = rb * 128 + (tid >> 2);
   const int64_t off = (e * N + row) * C + cb * 128 + (tid & 3) * 32;
 
-  // the bf16 intermediate, kept packed two values per register
-  uint32_t vp[16];
+  uint4 raw[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4*>(w_in + off + 16 * i);
+  // bf16(fp32(q) * scale) of bytes b and b + 1 of a word, packed
+  auto bf16_pair = [scale](uint32_t word, int b) {
+    const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_to_float((word >> (8 * b)) & 0xFFu) * scale,
+                                                    e4m3_to_float((word >> (8 * b + 8)) & 0xFFu) * scale);
+    return *reinterpret_cast<const uint32_t*>(&pr);
+  };
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(w_in + off + 16 * i);
-    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < 4; ++w)
 #pragma unroll
       for (int b = 0; b < 4; b += 2) {
-        const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_to_float((words[w] >> (8 * b)) & 0xFFu) * scale,
-                                                        e4m3_to_float((words[w] >> (8 * b + 8)) & 0xFFu) * scale);
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(&pr);
-        vp[i * 8 + w * 2 + b / 2] = u;
-        const float2 f = unpack_bf16x2(u);
+        const float2 f = unpack_bf16x2(bf16_pair(words[w], b));
         amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
       }
-    }
   }
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
@@ -71,12 +75,17 @@ __global__ void __launch_bounds__(kRequantThreads) requant_kernel(const uint8_t*
   for (int i = 1; i < kRequantThreads / 32; ++i) amax = fmaxf(amax, s_red[i]);
   const int s = ue8m0_exponent(amax);
   const float mul = exp2_neg(s);
+  // form the intermediate again rather than keep the first pass's values live
+  // across the reduction (an empty asm hides that the bytes are unchanged)
+#pragma unroll
+  for (int i = 0; i < 2; ++i) asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
+    const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
     uint32_t outw[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float2 lo = unpack_bf16x2(vp[i * 8 + w * 2]), hi = unpack_bf16x2(vp[i * 8 + w * 2 + 1]);
+      const float2 lo = unpack_bf16x2(bf16_pair(words[w], 0)), hi = unpack_bf16x2(bf16_pair(words[w], 2));
       outw[w] = cvt_e4m3x2(lo.x * mul, lo.y * mul) | (cvt_e4m3x2(hi.x * mul, hi.y * mul) << 16);
     }
     *reinterpret_cast<uint4*>(w_out + off + 16 * i) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
