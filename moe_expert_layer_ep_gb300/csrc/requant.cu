@@ -11,12 +11,13 @@
 //   v  = bf16(fp32(q) * s)                 (s: the block's fp32 scale)
 //   e  = smallest integer with amax|v| <= 448 * 2^e, clamped to [-127, 127]
 //   q' = e4m3(v * 2^-e)                    (round to nearest even, saturating)
-// One CTA per block: 512 threads, 32 bytes (a quarter row) each, read once,
-// reduced, written once; in-place operation (w_out == w_in) is allowed
-// because a CTA reads its whole block before writing it.  A thread keeps only
-// its 32 raw e4m3 bytes in registers and forms the bf16 intermediate twice
-// (for the block maximum, then for the output), the same arithmetic both
-// times: with few registers per thread, three blocks are in flight per SM.
+// One CTA per block: 256 threads, each two quarter rows (rows r and r + 64,
+// 32 bytes each), read once, reduced, written once; in-place operation
+// (w_out == w_in) is allowed because a CTA reads its whole block before
+// writing it.  A thread keeps only its 64 raw e4m3 bytes in registers and
+// forms the bf16 intermediate twice (for the block maximum, then for the
+// output), the same arithmetic both times: with few registers per thread,
+// five blocks are in flight per SM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,14 +25,15 @@ namespace moe {
 
 namespace {
 
-constexpr int kRequantThreads = 512;
+constexpr int kRequantThreads = 256;
+constexpr int kRequantParts = 2;     // quarter rows per thread
 
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
   return __half2float(__half(hr));
 }
 
-__global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8_t* w_in, const float* s_in,
+__global__ void __launch_bounds__(kRequantThreads, 5) requant_kernel(const uint8_t* w_in, const float* s_in,
                                                                  uint8_t* w_out, uint8_t* s_out, int64_t N,
                                                                  int64_t C) {
   __shared__ float s_red[kRequantThreads / 32];
@@ -43,11 +45,14 @@ __global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8
   const float scale = s_in[blk];
   const int tid = threadIdx.x;
   const int64_t row = rb * 128 + (tid >> 2);
+  // part p: row + 64 p, 16-byte halves h: raw[2 p + h]
   const int64_t off = (e * N + row) * C + cb * 128 + (tid & 3) * 32;
+  const int64_t part_stride = 64 * C;
 
-  uint4 raw[2];
+  uint4 raw[2 * kRequantParts];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) raw[i] = *reinterpret_cast<const uint4*>(w_in + off + 16 * i);
+  for (int i = 0; i < 2 * kRequantParts; ++i)
+    raw[i] = *reinterpret_cast<const uint4*>(w_in + off + (i >> 1) * part_stride + 16 * (i & 1));
   // bf16(fp32(q) * scale) of bytes b and b + 1 of a word, packed
   auto bf16_pair = [scale](uint32_t word, int b) {
     const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_to_float((word >> (8 * b)) & 0xFFu) * scale,
@@ -56,7 +61,7 @@ __global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8
   };
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 2 * kRequantParts; ++i) {
     const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
 #pragma unroll
     for (int w = 0; w < 4; ++w)
@@ -78,9 +83,10 @@ __global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8
   // form the intermediate again rather than keep the first pass's values live
   // across the reduction (an empty asm hides that the bytes are unchanged)
 #pragma unroll
-  for (int i = 0; i < 2; ++i) asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
+  for (int i = 0; i < 2 * kRequantParts; ++i)
+    asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < 2 * kRequantParts; ++i) {
     const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
     uint32_t outw[4];
 #pragma unroll
@@ -88,7 +94,8 @@ __global__ void __launch_bounds__(kRequantThreads, 3) requant_kernel(const uint8
       const float2 lo = unpack_bf16x2(bf16_pair(words[w], 0)), hi = unpack_bf16x2(bf16_pair(words[w], 2));
       outw[w] = cvt_e4m3x2(lo.x * mul, lo.y * mul) | (cvt_e4m3x2(hi.x * mul, hi.y * mul) << 16);
     }
-    *reinterpret_cast<uint4*>(w_out + off + 16 * i) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+    *reinterpret_cast<uint4*>(w_out + off + (i >> 1) * part_stride + 16 * (i & 1)) =
+        make_uint4(outw[0], outw[1], outw[2], outw[3]);
   }
   if (tid == 0) s_out[blk] = static_cast<uint8_t>(s + 127);
 }
