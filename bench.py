@@ -387,10 +387,14 @@ def gemm_roofline(name, flops, nbytes, ms, peaks, fp8):
     else:
         roof = {"bound": "tensor", "achieved": round(tf, 1), "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": round(tf / tensor_peak, 4)}
+    sustained = peaks["bf16_tflops_sustained"] * (2.0 if fp8 else 1.0)
     roof.update({"kernel": name, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                  "algorithmic_tflop": round(flops / 1e12, 4), "tflops": round(tf, 1),
                  "tensor_frac": round(tf / tensor_peak, 4), "hbm_gbs": round(gbs, 1),
                  "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                 # the same TFLOP/s against the measured sustained (power-capped) peak, the regime the
+                 # clock record shows when sw_power_cap is active during the timed region
+                 "tensor_frac_of_sustained": round(tf / sustained, 4),
                  "peak_source": peaks["source"] + (" (burst bf16 x 2 for fp8)" if fp8 else " (burst bf16)")})
     return roof
 

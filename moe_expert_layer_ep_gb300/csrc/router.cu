@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
+  // x may come from the previous kernel of the stream; the partial buffer
+  // may still be read by the previous call's top-k kernel
+  pdl_wait();
+  pdl_trigger();
   const int64_t n_items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * r.segs;
 
   if (warp == 0) {
@@ -282,6 +286,8 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* partial,
   static_assert(P <= 32, "taken mask is 32 bits");
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  pdl_wait();      // the logits kernel's partial sums are complete and visible
+  pdl_trigger();
   if (t >= T) return;
   float v[P];
   // logits = the segments' partial sums folded in segment order
@@ -368,18 +374,19 @@ cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, con
   }
   cudaError_t e = cudaMemsetAsync(r.status, 0, 16, s);
   if (e != cudaSuccess) return e;
-  router_logits_tc_kernel<<<grid, kRtThreads, kRtSmemBytes, s>>>(map_x, map_w, r);
+  e = launch_pdl(router_logits_tc_kernel, dim3(grid), dim3(kRtThreads), kRtSmemBytes, s, map_x, map_w, r);
+  if (e != cudaSuccess) return e;
   const int warps = 8;
-  const unsigned nb = static_cast<unsigned>((r.T + warps - 1) / warps);
-  if (r.E <= 128)
-    topk_softmax_kernel<4><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
-  else if (r.E <= 256)
-    topk_softmax_kernel<8><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
-  else if (r.E <= 512)
-    topk_softmax_kernel<16><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
-  else
-    topk_softmax_kernel<32><<<nb, warps * 32, 0, s>>>(r.partial, r.segs, r.T, r.E, topk, logits, ids, wts);
-  return cudaGetLastError();
+  const dim3 nb(static_cast<unsigned>((r.T + warps - 1) / warps)), block(warps * 32);
+  const int segs = r.segs;
+  const int E = r.E;
+  const int64_t T = r.T;
+  const float* partial = r.partial;
+  if (r.E <= 128) return launch_pdl(topk_softmax_kernel<4>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
+  if (r.E <= 256) return launch_pdl(topk_softmax_kernel<8>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
+  if (r.E <= 512)
+    return launch_pdl(topk_softmax_kernel<16>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
+  return launch_pdl(topk_softmax_kernel<32>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
 }
 
 }  // namespace moe

@@ -81,9 +81,19 @@ def test_masked_and_compact_agree(dtype, K, I, T):
         assert rel_fro(bf16_to_f64(om), bf16_to_f64(oc)) <= TOL
 
 
-def test_repeat_runs_bitwise_and_graph_replay():
-    p = Problem(T=257, K=512, I=256, E_global=16, E_local=16, topk=4, dtype="fp8", layout="compact", seed=3)
+@pytest.mark.parametrize("case", [dict(T=257, K=512, I=256, E_global=16, E_local=16, topk=4, dtype="fp8",
+                                       layout="compact", seed=3),
+                                  dict(T=48, K=1024, I=512, E_global=64, E_local=16, topk=8, dtype="fp8",
+                                       layout="masked", expert_start=16, seed=4)],
+                         ids=["compact", "masked-split"])
+def test_repeat_runs_bitwise_and_graph_replay(case):
+    """Repeated forwards give the same bits, and so does a CUDA-graph replay
+    (whose kernels overlap by programmatic dependent launch); the masked
+    case runs both GEMMs in K segments with their reduction kernels."""
+    p = Problem(**case)
     g = p.gpu()
+    if case["layout"] == "masked":
+        assert g.ctx.ws_layout.k_splits1 > 1 and g.ctx.ws_layout.k_splits2 > 1
     first = g.forward().clone()
     for _ in range(3):
         assert torch.equal(g.forward().view(torch.int16), first.view(torch.int16))
@@ -174,14 +184,16 @@ def test_mx_masked_decode_full_size_sampled(T, dtype):
     _sampled_check(p, g, sorted({0, T - 1}))
 
 
-@pytest.mark.parametrize("case", [dict(T=40, layout="masked", E_global=64, E_local=8),
-                                  dict(T=600, layout="compact", E_global=16, E_local=16)])
+@pytest.mark.parametrize("case", [dict(T=40, layout="masked", E_global=64, E_local=8, K=256, I=128),
+                                  dict(T=600, layout="compact", E_global=16, E_local=16, K=256, I=128),
+                                  dict(T=40, layout="masked", E_global=64, E_local=8, K=1024, I=512)])
 def test_forward_launch_count_matches_profiler(case):
     """moe_forward_launches (what the bench reports as gpu_launches) equals the
-    libmoe kernels a profiler sees in one forward (small and large plans)."""
+    libmoe kernels a profiler sees in one forward (small and large plans, and
+    a masked layout whose GEMMs add their split-K reduction kernels)."""
     import moe_expert_layer_ep_gb300 as M
     profiler = pytest.importorskip("torch.profiler")
-    p = Problem(K=256, I=128, topk=8, dtype="fp8", **case)
+    p = Problem(topk=8, dtype="fp8", **case)
     g = p.gpu()
     g.forward()
     torch.cuda.synchronize()
