@@ -426,7 +426,10 @@ moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, vo
   return cuda_status(moe::launch_plan(p, static_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void* stream) {
+// topk_ids: given by moe_forward, whose small problems then quantise with
+// destinations formed from the routing, beside the plan (launch_quant_scatter).
+static moe_status_t quant_scatter(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids, void* ws,
+                                  void* stream) {
   moe_status_t st = check_ws(ctx, ws);
   if (st != MOE_OK) return st;
   const moe_shape_t& s = ctx->shape;
@@ -446,7 +449,15 @@ moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void*
   q.blocks_per_expert = static_cast<int32_t>((s.max_m + 127) / 128);
   q.a = at<void>(ws, ctx->ws.a);
   q.a_sf = at<uint8_t>(ws, ctx->ws.a_sf);
+  q.topk_ids = topk_ids;
+  q.E_global = s.E_global;
+  q.E_local = s.E_local;
+  q.expert_start = s.expert_start;
   return cuda_status(moe::launch_quant_scatter(q, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void* stream) {
+  return quant_scatter(ctx, x_bf16, nullptr, ws, stream);
 }
 
 static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
@@ -495,7 +506,7 @@ moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_i
                          void* ws, void* out_bf16, void* stream) {
   moe_status_t st;
   if ((st = moe_plan_layout(ctx, topk_ids, ws, stream)) != MOE_OK) return st;
-  if ((st = moe_quant_scatter(ctx, x_bf16, ws, stream)) != MOE_OK) return st;
+  if ((st = quant_scatter(ctx, x_bf16, topk_ids, ws, stream)) != MOE_OK) return st;
   if ((st = moe_grouped_gemm_w13_act(ctx, ws, stream)) != MOE_OK) return st;
   if ((st = moe_grouped_gemm_w2(ctx, ws, stream)) != MOE_OK) return st;
   return moe_combine(ctx, topk_weights, ws, out_bf16, stream);

@@ -64,6 +64,10 @@ struct PlanArgs {
 struct QuantArgs {
   const void* x;            // bf16 [T, K]
   const int32_t* src2dst;   // [T, topk]
+  // small problems (plan_is_small): the kernel forms each token's
+  // destinations itself from the routing, by the plan's rule
+  const int32_t* topk_ids;  // [T, topk]
+  int32_t E_global, E_local, expert_start;
   int64_t T, K;
   int32_t topk;
   int32_t fp8;
@@ -120,6 +124,11 @@ struct GemmArgs {
   int64_t part_cols;          // n_blocks * 256
 };
 
+// Problems the one-CTA plan handles: at most kPlanSmallMaxA assignments and
+// kPlanSmallMaxE local experts.
+constexpr int kPlanSmallMaxA = 2048;
+constexpr int kPlanSmallMaxE = 256;
+inline bool plan_is_small(int64_t A, int32_t E_local) { return A <= kPlanSmallMaxA && E_local <= kPlanSmallMaxE; }
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
 int plan_launch_count(int64_t A, int32_t E_local);   // kernels one launch_plan enqueues
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);

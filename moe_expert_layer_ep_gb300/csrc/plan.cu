@@ -266,8 +266,6 @@ __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
 // is the expert's count in earlier chunks + in earlier warps of its chunk +
 // in earlier lanes of its warp (warp match), as in the three-kernel path, so
 // the outputs are identical to it.
-constexpr int kPlanSmallMaxA = 2048;
-constexpr int kPlanSmallMaxE = 256;
 
 __global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
   __shared__ int s_wcnt[32 * kPlanSmallMaxE];   // [warp][expert] counts of the current chunk
@@ -337,7 +335,6 @@ __global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
 
 }  // namespace
 
-bool plan_is_small(int64_t A, int32_t E_local) { return A <= kPlanSmallMaxA && E_local <= kPlanSmallMaxE; }
 
 int plan_launch_count(int64_t A, int32_t E_local) {
   if (plan_is_small(A, E_local)) return 1;

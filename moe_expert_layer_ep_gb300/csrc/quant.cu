@@ -38,31 +38,14 @@ __device__ __forceinline__ void dest_block(const QuantArgs& q, int64_t d, int64_
   }
 }
 
+// One token row: read once (16-byte loads, 8 columns per thread), quantised
+// once, written to each destination row listed in s_dst (-1: none).
 // kMX: MXFP8, one exponent per 32 columns (4 lanes); the four exponents of a
 // 128-column group fill the four bytes of the row's scale word.
 template <bool kFP8, bool kMX>
-__global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs q) {
-  __shared__ int64_t s_dst[kMaxTopk];
-  __shared__ int64_t s_blk[kMaxTopk];
-  __shared__ int s_row[kMaxTopk];
-  __shared__ int s_any;
-  const int64_t t = blockIdx.x;
+__device__ __forceinline__ void quant_scatter_row(const QuantArgs& q, int64_t t, const int64_t* s_dst,
+                                                  const int64_t* s_blk, const int* s_row) {
   const int tid = threadIdx.x;
-  if (tid == 0) s_any = 0;
-  pdl_wait();
-  pdl_trigger();
-  __syncthreads();
-  if (tid < q.topk) {
-    const int64_t d = q.src2dst[t * q.topk + tid];
-    s_dst[tid] = d;
-    if (d >= 0) {
-      s_any = 1;
-      dest_block(q, d, &s_blk[tid], &s_row[tid]);
-    }
-  }
-  __syncthreads();
-  if (!s_any) return;
-
   const uint16_t* xrow = static_cast<const uint16_t*>(q.x) + t * q.K;
   const int64_t n_groups = q.K / 128;
   for (int64_t c0 = 0; c0 < q.K; c0 += kColsPerIter) {
@@ -120,6 +103,94 @@ __global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs 
       }
     }
   }
+}
+
+template <bool kFP8, bool kMX>
+__global__ void __launch_bounds__(kQuantThreads) quant_scatter_kernel(QuantArgs q) {
+  __shared__ int64_t s_dst[kMaxTopk];
+  __shared__ int64_t s_blk[kMaxTopk];
+  __shared__ int s_row[kMaxTopk];
+  __shared__ int s_any;
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_any = 0;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  if (tid < q.topk) {
+    const int64_t d = q.src2dst[t * q.topk + tid];
+    s_dst[tid] = d;
+    if (d >= 0) {
+      s_any = 1;
+      dest_block(q, d, &s_blk[tid], &s_row[tid]);
+    }
+  }
+  __syncthreads();
+  if (!s_any) return;
+  quant_scatter_row<kFP8, kMX>(q, t, s_dst, s_blk, s_row);
+}
+
+// Small problems inside moe_forward (at most kPlanSmallMaxA assignments and
+// kPlanSmallMaxE local experts): each CTA forms its token's destination rows
+// itself, by the plan's rule (the stable rank of the assignment among its
+// expert's assignments in flattened t * topk + j order; compact: after the
+// earlier experts' 128-padded segments; masked: e * max_m + rank, dropped
+// past max_m), so it runs beside the one-CTA plan instead of after it.  It
+// waits for the plan to complete only before it finishes, so the kernels
+// after it see the plan's tables complete.
+template <bool kFP8, bool kMX>
+__global__ void __launch_bounds__(kQuantThreads) quant_scatter_small_kernel(QuantArgs q) {
+  __shared__ int16_t s_lid[kPlanSmallMaxA];   // local expert of every assignment, -1: not local
+  __shared__ int s_cnt[kPlanSmallMaxE];       // compact: assignments per local expert
+  __shared__ int64_t s_dst[kMaxTopk];
+  __shared__ int64_t s_blk[kMaxTopk];
+  __shared__ int s_row[kMaxTopk];
+  __shared__ int s_any;
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t A = q.T * q.topk;
+  for (int x = tid; x < q.E_local; x += kQuantThreads) s_cnt[x] = 0;
+  if (tid == 0) s_any = 0;
+  __syncthreads();
+  for (int64_t i = tid; i < A; i += kQuantThreads) {
+    const int32_t gid = q.topk_ids[i];
+    const int e = (gid >= 0 && gid < q.E_global) ? gid - q.expert_start : -1;
+    const int lid = (e >= 0 && e < q.E_local) ? e : -1;
+    s_lid[i] = static_cast<int16_t>(lid);
+    if (!q.masked && lid >= 0) atomicAdd(&s_cnt[lid], 1);
+  }
+  __syncthreads();
+  for (int j = warp; j < q.topk; j += kQuantThreads / 32) {
+    const int64_t pos = t * q.topk + j;
+    const int e = s_lid[pos];
+    int rank = 0;
+    if (e >= 0)
+      for (int64_t i = lane; i < pos; i += 32) rank += s_lid[i] == e;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    if (lane == 0) {
+      int64_t d = -1;
+      if (e >= 0) {
+        if (q.masked) {
+          if (rank < q.max_m) d = static_cast<int64_t>(e) * q.max_m + rank;
+        } else {
+          int64_t start = 0;
+          for (int x = 0; x < e; ++x) start += (s_cnt[x] + kBlockM - 1) / kBlockM * kBlockM;
+          d = start + rank;
+        }
+      }
+      s_dst[j] = d;
+      if (d >= 0) {
+        s_any = 1;
+        dest_block(q, d, &s_blk[j], &s_row[j]);
+      }
+    }
+  }
+  __syncthreads();
+  if (s_any) quant_scatter_row<kFP8, kMX>(q, t, s_dst, s_blk, s_row);
+  // finish only after the plan (the previous kernel) has completed
+  pdl_wait();
+  pdl_trigger();
 }
 
 constexpr int kCombineThreads = 256;
@@ -183,6 +254,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs c)
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s) {
   if (q.T <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(q.T)), block(kQuantThreads);
+  if (q.topk_ids && plan_is_small(q.T * q.topk, q.E_local)) {
+    if (q.mx) return launch_pdl(quant_scatter_small_kernel<true, true>, grid, block, 0, s, q);
+    if (q.fp8) return launch_pdl(quant_scatter_small_kernel<true, false>, grid, block, 0, s, q);
+    return launch_pdl(quant_scatter_small_kernel<false, false>, grid, block, 0, s, q);
+  }
   if (q.mx) return launch_pdl(quant_scatter_kernel<true, true>, grid, block, 0, s, q);
   if (q.fp8) return launch_pdl(quant_scatter_kernel<true, false>, grid, block, 0, s, q);
   return launch_pdl(quant_scatter_kernel<false, false>, grid, block, 0, s, q);

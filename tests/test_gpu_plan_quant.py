@@ -113,3 +113,35 @@ def test_quant_edge_values_fp8():
     got = g.view("a").index_select(0, torch.as_tensor(rows, device="cuda")).cpu().numpy()
     assert np.array_equal(got, oracle.e4m3_bits(q))
     assert np.array_equal(g.sf_bytes("a_sf", rows), (s + 127).astype(np.uint8))
+
+
+SMALL_FORWARD_CASES = [c for c in CASES if 0 < c["T"] * c["topk"] <= 2048 and c["E_local"] <= 256]
+
+
+@pytest.mark.parametrize("case", SMALL_FORWARD_CASES, ids=[_ids(c) for c in SMALL_FORWARD_CASES])
+def test_forward_quant_destinations_match_the_plan(case):
+    """Inside moe_forward, small problems quantise with destination rows the
+    quant kernel forms from the routing itself (beside the plan, not after
+    it).  Its expert rows and scales must be the bytes the plan-driven
+    moe_quant_scatter writes, and its src2dst the plan's."""
+    p = Problem(**case, weight_device="cpu")
+    ref = p.gpu()
+    ref.plan()
+    ref.quant()
+    torch.cuda.synchronize()
+    fwd = p.gpu()
+    fwd.forward()
+    torch.cuda.synchronize()
+    assert fwd.status() == 0
+    src = ref.view("src2dst").cpu().numpy()
+    assert np.array_equal(fwd.view("src2dst").cpu().numpy(), src)
+    rows = np.sort(src[src >= 0])
+    if rows.size == 0:
+        return
+    idx = torch.as_tensor(rows, device="cuda")
+    a_ref, a_fwd = ref.view("a").index_select(0, idx), fwd.view("a").index_select(0, idx)
+    if p.dtype == "bf16":
+        assert torch.equal(a_ref.view(torch.int16), a_fwd.view(torch.int16))
+    else:
+        assert torch.equal(a_ref, a_fwd)
+        assert np.array_equal(ref.sf_bytes("a_sf", rows), fwd.sf_bytes("a_sf", rows))
