@@ -14,10 +14,19 @@
 // One CTA per block: 256 threads, each two quarter rows (rows r and r + 64,
 // 32 bytes each), read once, reduced, written once; in-place operation
 // (w_out == w_in) is allowed because a CTA reads its whole block before
-// writing it.  A thread keeps only its 64 raw e4m3 bytes in registers and
-// forms the bf16 intermediate twice (for the block maximum, then for the
-// output), the same arithmetic both times: with few registers per thread,
-// five blocks are in flight per SM.
+// writing it.
+//   amax: |v| = bf16(fp32(|q|) * |s|) (both roundings are odd-symmetric)
+//         is non-decreasing in |q|, and the magnitude bits of a finite e4m3
+//         code (byte & 0x7f) order like |q|, so amax|v| is that function of
+//         the block's largest magnitude byte: four bytes per byte-wise
+//         integer max, one conversion per block.
+//   q':   two codes per conversion (e4m3x2 -> f16x2 -> two fp32), the two
+//         products of each pair in one packed fp32 multiply, both roundings
+//         to bf16 in one conversion, the power-of-two rescale again as one
+//         packed multiply (exact) and one two-code conversion back.
+// About five instructions per byte and 32 registers per thread, so eight
+// blocks (128 KB of loads) are in flight per SM and the kernel streams at
+// close to HBM speed instead of waiting on its arithmetic.
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,68 +42,79 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
   return __half2float(__half(hr));
 }
 
-__global__ void __launch_bounds__(kRequantThreads, 5) requant_kernel(const uint8_t* w_in, const float* s_in,
+// (a, b) * (m, m) in one packed fp32 multiply, round to nearest even
+__device__ __forceinline__ float2 mul_f32x2(float a, float b, float m) {
+  float2 r;
+  asm("{\n\t.reg .b64 p, q, m2;\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 m2, {%4, %4};\n\t"
+      "mul.rn.f32x2 q, p, m2;\n\t"
+      "mov.b64 {%0, %1}, q;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a), "f"(b), "f"(m));
+  return r;
+}
+
+// two e4m3 codes (low 16 bits of pair) -> e4m3(bf16(fp32(q) * s) * 2^-e), lo first
+__device__ __forceinline__ uint32_t requant_pair(uint32_t pair, float s, float mul) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair), __NV_E4M3);
+  const float2 q = __half22float2(__half2(h));
+  const float2 p = mul_f32x2(q.x, q.y, s);              // fp32 products
+  const float2 v = unpack_bf16x2(pack_bf16x2(p.x, p.y));    // the bf16 intermediate
+  const float2 r = mul_f32x2(v.x, v.y, mul);            // exact power-of-two rescale
+  return cvt_e4m3x2(r.x, r.y);
+}
+
+__global__ void __launch_bounds__(kRequantThreads, 8) requant_kernel(const uint8_t* w_in, const float* s_in,
                                                                  uint8_t* w_out, uint8_t* s_out, int64_t N,
                                                                  int64_t C) {
-  __shared__ float s_red[kRequantThreads / 32];
-  const int64_t nbn = N / 128, nbc = C / 128;
+  __shared__ uint32_t s_red[kRequantThreads / 32];
+  // blocks in (expert, row block, column block) order: block b starts at row
+  // 128 (b / (C / 128)) of the [E * N, C] byte matrix, column 128 (b % (C / 128))
+  const int64_t nbc = C / 128;
   const int64_t blk = blockIdx.x;
-  const int64_t e = blk / (nbn * nbc);
-  const int64_t rb = (blk / nbc) % nbn;
-  const int64_t cb = blk % nbc;
   const float scale = s_in[blk];
   const int tid = threadIdx.x;
-  const int64_t row = rb * 128 + (tid >> 2);
   // part p: row + 64 p, 16-byte halves h: raw[2 p + h]
-  const int64_t off = (e * N + row) * C + cb * 128 + (tid & 3) * 32;
   const int64_t part_stride = 64 * C;
+  const uint8_t* src = w_in + ((blk / nbc) * 128 + (tid >> 2)) * C + (blk % nbc) * 128 + (tid & 3) * 32;
 
   uint4 raw[2 * kRequantParts];
 #pragma unroll
   for (int i = 0; i < 2 * kRequantParts; ++i)
-    raw[i] = *reinterpret_cast<const uint4*>(w_in + off + (i >> 1) * part_stride + 16 * (i & 1));
-  // bf16(fp32(q) * scale) of bytes b and b + 1 of a word, packed
-  auto bf16_pair = [scale](uint32_t word, int b) {
-    const __nv_bfloat162 pr = __floats2bfloat162_rn(e4m3_to_float((word >> (8 * b)) & 0xFFu) * scale,
-                                                    e4m3_to_float((word >> (8 * b + 8)) & 0xFFu) * scale);
-    return *reinterpret_cast<const uint32_t*>(&pr);
-  };
-  float amax = 0.0f;
+    raw[i] = *reinterpret_cast<const uint4*>(src + (i >> 1) * part_stride + 16 * (i & 1));
+  // the block's largest magnitude code
+  uint32_t mw = 0;
 #pragma unroll
   for (int i = 0; i < 2 * kRequantParts; ++i) {
-    const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-#pragma unroll
-      for (int b = 0; b < 4; b += 2) {
-        const float2 f = unpack_bf16x2(bf16_pair(words[w], b));
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
+    const uint32_t a = __vmaxu4(raw[i].x & 0x7F7F7F7Fu, raw[i].y & 0x7F7F7F7Fu);
+    const uint32_t b = __vmaxu4(raw[i].z & 0x7F7F7F7Fu, raw[i].w & 0x7F7F7F7Fu);
+    mw = __vmaxu4(mw, __vmaxu4(a, b));
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-  if ((tid & 31) == 0) s_red[tid >> 5] = amax;
+  mw = __vmaxu4(mw, mw >> 16);
+  mw = __vmaxu4(mw, mw >> 8) & 0xFFu;
+  mw = __reduce_max_sync(0xFFFFFFFFu, mw);
+  if ((tid & 31) == 0) s_red[tid >> 5] = mw;
   __syncthreads();
-  amax = s_red[0];
+  mw = s_red[0];
 #pragma unroll
-  for (int i = 1; i < kRequantThreads / 32; ++i) amax = fmaxf(amax, s_red[i]);
+  for (int i = 1; i < kRequantThreads / 32; ++i) mw = max(mw, s_red[i]);
+  const float amax = unpack_bf16x2(pack_bf16x2(e4m3_to_float(mw) * fabsf(scale), 0.0f)).x;
   const int s = ue8m0_exponent(amax);
   const float mul = exp2_neg(s);
-  // form the intermediate again rather than keep the first pass's values live
-  // across the reduction (an empty asm hides that the bytes are unchanged)
-#pragma unroll
-  for (int i = 0; i < 2 * kRequantParts; ++i)
-    asm volatile("" : "+r"(raw[i].x), "+r"(raw[i].y), "+r"(raw[i].z), "+r"(raw[i].w));
+  // the output address formed again here rather than kept live across the
+  // reduction (an empty asm hides that the thread index is unchanged)
+  int t2 = tid;
+  asm volatile("" : "+r"(t2));
+  uint8_t* dst = w_out + ((blk / nbc) * 128 + (t2 >> 2)) * C + (blk % nbc) * 128 + (t2 & 3) * 32;
 #pragma unroll
   for (int i = 0; i < 2 * kRequantParts; ++i) {
     const uint32_t words[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
     uint32_t outw[4];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float2 lo = unpack_bf16x2(bf16_pair(words[w], 0)), hi = unpack_bf16x2(bf16_pair(words[w], 2));
-      outw[w] = cvt_e4m3x2(lo.x * mul, lo.y * mul) | (cvt_e4m3x2(hi.x * mul, hi.y * mul) << 16);
-    }
-    *reinterpret_cast<uint4*>(w_out + off + (i >> 1) * part_stride + 16 * (i & 1)) =
+    for (int w = 0; w < 4; ++w)
+      outw[w] = requant_pair(words[w] & 0xFFFFu, scale, mul) | (requant_pair(words[w] >> 16, scale, mul) << 16);
+    *reinterpret_cast<uint4*>(dst + (i >> 1) * part_stride + 16 * (i & 1)) =
         make_uint4(outw[0], outw[1], outw[2], outw[3]);
   }
   if (tid == 0) s_out[blk] = static_cast<uint8_t>(s + 127);

@@ -32,6 +32,25 @@ def test_requant_bit_exact(E, N, C):
     assert np.array_equal(out_s.cpu().numpy().astype(np.int64) - 127, ref_e)
 
 
+def test_requant_signed_and_extreme_scales_bit_exact():
+    """Negative scales (the block maximum is taken over |v|), zero, scales
+    whose products fall below the fp32 normal range (exponent clamped at
+    -127) and scales whose products approach the fp32 maximum."""
+    w, s = _case(2, 256, 512, 23)
+    s = s.clone()
+    s[0, 0, :] = -s[0, 0, :]
+    s[0, 1, 0] = -0.0
+    s[1, 0, 0] = 2.0 ** -140                         # products below the fp32 normal range
+    s[1, 0, 1] = 2.0 ** 100                          # large exponents (finite products)
+    s[1, 1, 2] = -(2.0 ** -100)
+    s[1, 1, 3] = 3.0e38 / 448.0
+    ref_w, ref_e = RQ.requant_block_ue8m0(w.numpy(), s.numpy())
+    out_w, out_s = M.moe_requant_weights_ue8m0(w.cuda(), s.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(out_w.cpu().numpy(), ref_w)
+    assert np.array_equal(out_s.cpu().numpy().astype(np.int64) - 127, ref_e)
+
+
 def test_requant_in_place_matches():
     w, s = _case(2, 256, 256, 3)
     a = w.cuda()
