@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 constexpr int kColsPerIter = kQuantThreads * 8;
+constexpr int kLoadBatch = 4;
 
 __device__ __forceinline__ void dest_block(const QuantArgs& q, int64_t d, int64_t* block, int* row) {
   if (!q.masked) {
@@ -48,57 +49,69 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& q, int64_t t,
   const int tid = threadIdx.x;
   const uint16_t* xrow = static_cast<const uint16_t*>(q.x) + t * q.K;
   const int64_t n_groups = q.K / 128;
-  for (int64_t c0 = 0; c0 < q.K; c0 += kColsPerIter) {
-    const int64_t col = c0 + static_cast<int64_t>(tid) * 8;
-    const bool active = col < q.K;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (active) v = __ldg(reinterpret_cast<const uint4*>(xrow + col));
-    if constexpr (kFP8) {
-      float f[8];
-      const float2 p0 = unpack_bf16x2(v.x), p1 = unpack_bf16x2(v.y), p2 = unpack_bf16x2(v.z),
-                   p3 = unpack_bf16x2(v.w);
-      f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
-      f[4] = p2.x; f[5] = p2.y; f[6] = p3.x; f[7] = p3.y;
-      float amax = 0.0f;
+  // kLoadBatch row segments per thread are loaded before any is used
+  for (int64_t c1 = 0; c1 < q.K; c1 += kLoadBatch * kColsPerIter) {
+    uint4 vb[kLoadBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      // 16 lanes = one 128-column group (MXFP8: 4 lanes = one 32-column block)
+    for (int b = 0; b < kLoadBatch; ++b) {
+      const int64_t col = c1 + b * kColsPerIter + static_cast<int64_t>(tid) * 8;
+      vb[b] = make_uint4(0, 0, 0, 0);
+      if (col < q.K) vb[b] = __ldg(reinterpret_cast<const uint4*>(xrow + col));
+    }
 #pragma unroll
-      for (int o = kMX ? 2 : 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-      const int s = ue8m0_exponent(amax);
-      uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
-      if constexpr (kMX) {
-        const int lane = tid & 31;
-        const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 4);
-        const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 8);
-        const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 12);
-        sf_word = static_cast<uint32_t>(s + 127) | (b1 << 8) | (b2 << 16) | (b3 << 24);   // valid at group leads
-      }
-      const float mul = exp2_neg(s);
-      uint2 packed;
-      packed.x = cvt_e4m3x2(f[0] * mul, f[1] * mul) | (cvt_e4m3x2(f[2] * mul, f[3] * mul) << 16);
-      packed.y = cvt_e4m3x2(f[4] * mul, f[5] * mul) | (cvt_e4m3x2(f[6] * mul, f[7] * mul) << 16);
-      if (active) {
-        const int64_t group = col >> 7;
-        const bool group_lead = (tid & 15) == 0;
-        for (int j = 0; j < q.topk; ++j) {
-          const int64_t d = s_dst[j];
-          if (d < 0) continue;
-          uint8_t* arow = static_cast<uint8_t*>(q.a) + d * q.K;
-          *reinterpret_cast<uint2*>(arow + col) = packed;
-          if (group_lead) {
-            *reinterpret_cast<uint32_t*>(q.a_sf + sf_chunk_offset(s_blk[j], group, n_groups) +
-                                         sf_row_offset(s_row[j])) = sf_word;
+    for (int b = 0; b < kLoadBatch; ++b) {
+      const int64_t c0 = c1 + b * kColsPerIter;
+      if (c0 >= q.K) break;                 // uniform over the CTA
+      const int64_t col = c0 + static_cast<int64_t>(tid) * 8;
+      const bool active = col < q.K;
+      const uint4 v = vb[b];
+      if constexpr (kFP8) {
+        float f[8];
+        const float2 p0 = unpack_bf16x2(v.x), p1 = unpack_bf16x2(v.y), p2 = unpack_bf16x2(v.z),
+                     p3 = unpack_bf16x2(v.w);
+        f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
+        f[4] = p2.x; f[5] = p2.y; f[6] = p3.x; f[7] = p3.y;
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        // 16 lanes = one 128-column group (MXFP8: 4 lanes = one 32-column block)
+#pragma unroll
+        for (int o = kMX ? 2 : 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const int s = ue8m0_exponent(amax);
+        uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
+        if constexpr (kMX) {
+          const int lane = tid & 31;
+          const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 4);
+          const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 8);
+          const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 12);
+          sf_word = static_cast<uint32_t>(s + 127) | (b1 << 8) | (b2 << 16) | (b3 << 24);   // valid at group leads
+        }
+        const float mul = exp2_neg(s);
+        uint2 packed;
+        packed.x = cvt_e4m3x2(f[0] * mul, f[1] * mul) | (cvt_e4m3x2(f[2] * mul, f[3] * mul) << 16);
+        packed.y = cvt_e4m3x2(f[4] * mul, f[5] * mul) | (cvt_e4m3x2(f[6] * mul, f[7] * mul) << 16);
+        if (active) {
+          const int64_t group = col >> 7;
+          const bool group_lead = (tid & 15) == 0;
+          for (int j = 0; j < q.topk; ++j) {
+            const int64_t d = s_dst[j];
+            if (d < 0) continue;
+            uint8_t* arow = static_cast<uint8_t*>(q.a) + d * q.K;
+            *reinterpret_cast<uint2*>(arow + col) = packed;
+            if (group_lead) {
+              *reinterpret_cast<uint32_t*>(q.a_sf + sf_chunk_offset(s_blk[j], group, n_groups) +
+                                           sf_row_offset(s_row[j])) = sf_word;
+            }
           }
         }
-      }
-    } else {
-      if (active) {
-        for (int j = 0; j < q.topk; ++j) {
-          const int64_t d = s_dst[j];
-          if (d < 0) continue;
-          uint16_t* arow = static_cast<uint16_t*>(q.a) + d * q.K;
-          *reinterpret_cast<uint4*>(arow + col) = v;
+      } else {
+        if (active) {
+          for (int j = 0; j < q.topk; ++j) {
+            const int64_t d = s_dst[j];
+            if (d < 0) continue;
+            uint16_t* arow = static_cast<uint16_t*>(q.a) + d * q.K;
+            *reinterpret_cast<uint4*>(arow + col) = v;
+          }
         }
       }
     }
