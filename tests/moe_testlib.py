@@ -17,7 +17,10 @@ def rel_fro(a, b):
 
 
 def bf16_to_f64(t):
-    return t.detach().float().cpu().numpy().astype(np.float64)
+    # whole stage buffers come through here, and their padding rows are left
+    # unwritten by design: a signalling NaN pattern there is not an error
+    with np.errstate(invalid="ignore"):
+        return t.detach().float().cpu().numpy().astype(np.float64)
 
 
 class Problem:
