@@ -34,6 +34,9 @@ struct moe_ctx {
   CUtensorMap map_a;
   CUtensorMap map_h;
   CUtensorMap map_y;   // GEMM2 output, 32-column store boxes
+  CUtensorMap map_a_half;   // compact: 64-row boxes of a and h (column-block pairs)
+  CUtensorMap map_h_half;
+  int pair_ctas[2];    // per GEMM stage: CTAs of a pair launch that fit at once (-1: not queried yet)
   uint64_t timeout_ns;
 };
 
@@ -61,16 +64,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // 3-D K-major tile map over [dim2][dim1][dim0] with a 128-byte inner box and
-// 128 rows, 128-byte swizzle (the layout the MMA descriptors expect).
+// box_rows rows, 128-byte swizzle (the layout the MMA descriptors expect).
 // store64: a 64-byte inner box with 64-byte swizzle (the GEMM2 output stores).
 moe_status_t make_map(CUtensorMap* map, const void* base, bool fp8, uint64_t dim0, uint64_t dim1, uint64_t dim2,
-                      bool store64 = false) {
+                      bool store64 = false, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return MOE_ERR_CUDA;
   const uint64_t esize = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {dim0, dim1, dim2};
   cuuint64_t strides[2] = {dim0 * esize, dim0 * dim1 * esize};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>((store64 ? 64 : 128) / esize), 128, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>((store64 ? 64 : 128) / esize), box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -260,6 +263,12 @@ moe_status_t ensure_ws_maps(moe_ctx* c, void* ws) {
     if (st != MOE_OK) return st;
     st = make_map(&c->map_y, at<uint8_t>(ws, c->ws.y), false, s.K, d1, d2, true);
     if (st != MOE_OK) return st;
+    if (!masked) {
+      st = make_map(&c->map_a_half, at<uint8_t>(ws, c->ws.a), c->fp8, s.K, d1, d2, false, 64);
+      if (st != MOE_OK) return st;
+      st = make_map(&c->map_h_half, at<uint8_t>(ws, c->ws.h), c->fp8, s.I, d1, d2, false, 64);
+      if (st != MOE_OK) return st;
+    }
   }
   c->ws_for_maps = ws;
   return MOE_OK;
@@ -363,6 +372,7 @@ moe_status_t moe_ctx_create(const moe_shape_t* shape, const void* w13, const uin
   c->w2 = w2;
   c->w2_sf = w2_sf;
   c->timeout_ns = 2000000000ull;
+  c->pair_ctas[0] = c->pair_ctas[1] = -1;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
     delete c;
@@ -466,12 +476,22 @@ static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
   if (ctx->ws.blocks == 0) return MOE_OK;
   st = ensure_ws_maps(ctx, ws);
   if (st != MOE_OK) return st;
-  const moe::GemmArgs g = gemm_args(ctx, ws, stage);
+  moe::GemmArgs g = gemm_args(ctx, ws, stage);
   int64_t max_tiles = ctx->ws.blocks * g.n_blocks * g.k_splits;
-  int grid = ctx->num_sms;
-  if (max_tiles < grid) grid = static_cast<int>(max_tiles);
+  // FP8 kinds, compact, unsplit, an even number of column blocks: column-block
+  // pairs share their A tile through cluster multicast (measured 1-2% faster
+  // per step on the FP8 prefills; no gain on BF16, which stays unpaired)
+  const bool pairable = g.fp8 && !g.masked && g.k_splits == 1 && g.n_blocks % 2 == 0;
+  int& pair_ctas = ctx->pair_ctas[stage - 1];
+  if (pairable && pair_ctas < 0) pair_ctas = moe::gemm_pair_ctas(g);
+  g.pair = pairable && pair_ctas >= 2;
+  int grid = g.pair ? (pair_ctas < ctx->num_sms ? pair_ctas : ctx->num_sms) & ~1 : ctx->num_sms;
+  if (max_tiles < grid) grid = static_cast<int>(max_tiles);   // (even when paired: n_blocks is)
   moe::GemmMaps m;
-  m.a = stage == 1 ? ctx->map_a : ctx->map_h;
+  if (g.pair)
+    m.a = stage == 1 ? ctx->map_a_half : ctx->map_h_half;
+  else
+    m.a = stage == 1 ? ctx->map_a : ctx->map_h;
   m.b = stage == 1 ? ctx->map_w13 : ctx->map_w2;
   m.out = stage == 1 ? ctx->map_a : ctx->map_y;   // stage 1 stores through plain writes
   m.wsf = ctx->mx ? (stage == 1 ? ctx->map_w13_sf : ctx->map_w2_sf) : m.b;   // (not read without MX scales)

@@ -51,6 +51,16 @@
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
 // path, whose other tensor-memory columns hold the scale tiles).
 //
+// Column-block pairs (g.pair: FP8 kinds, compact layout, no split, an even
+// number of column blocks): the kernel runs in clusters of two CTAs whose
+// work units are always column blocks 2m and 2m + 1 of one row block, so
+// they read the same A tile.  Each CTA's producer loads one 64-row half of it
+// with TMA multicast into both CTAs' stage (each CTA's barrier counts both
+// halves), and each CTA's MMA completion frees the stage in both CTAs, so a
+// stage is refilled only once both have read it.  Per CTA, half of the A
+// bytes (a sixth of all loaded bytes) leave L2; the MMAs, their operands and
+// so the results are those of the unpaired kernel.
+//
 // Every row is computed by the same instruction sequence with the same K
 // order whatever the batch, so results are batch-invariant and reproducible.
 // Rows of a block beyond its valid count (padding, -1 in m_indices) are
@@ -189,11 +199,15 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // column-block pair: this CTA loads half `crank` of the shared A tile for
+  // both CTAs, and a stage is free only once both CTAs' MMAs have read it
+  const bool pair = g.pair != 0;
+  const uint32_t crank = pair ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1 + scale_warps(kFP8, kMX));   // producer (+ scale warp)
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], pair ? 2 : 1);                // this CTA's MMAs (+ the partner's)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -214,7 +228,12 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // a pair's barriers are initialised in both CTAs before either CTA's copies
+  // or MMA completions can reach them
+  if (pair)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *holder;
 
@@ -285,7 +304,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
           // group unwritten and counts only the 16 KB of codes)
           mbar_arrive_expect_tx(&full[stage], bytes);
           const int kc = kb * kElemsPerKBlock;
-          tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
+          if (pair)   // 64 rows of A into both CTAs; the partner brings the other 64
+            tma_load_3d_multicast(smem + kOffA + stage * kABytes + crank * (kABytes / 2), &map_a, &full[stage], kc,
+                                  tl.tma_row + 64 * static_cast<int>(crank), a_e, 0x3);
+          else
+            tma_load_3d(smem + kOffA + stage * kABytes, &map_a, &full[stage], kc, tl.tma_row, a_e);
           // the whole B tile in one box: GEMM1 gate rows then up rows, GEMM2
           // 256 consecutive rows (MXFP4: the map counts 4-bit codes)
           uint8_t* bdst = smem + kOffB + stage * kBBytes;
@@ -377,7 +400,10 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
             for (int k = 0; k < 4; ++k)
               mma_bf16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescBF16, !(first && k == 0));
           }
-          tc_commit(&empty[stage]);
+          if (pair)
+            tc_commit_multicast(&empty[stage], 0x3);   // the stage's A halves live in both CTAs
+          else
+            tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -751,7 +777,12 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
   }
 
   if (kStage == 2 && warp == 2 && lane == 0) bulk_wait_all();   // the TMA stores of y have completed
-  __syncthreads();
+  // a pair leaves together: neither CTA's copies or MMA completions may still
+  // be on their way to the other's shared memory
+  if (pair)
+    cluster_sync();
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -768,8 +799,45 @@ cudaError_t launch_one(const GemmArgs& g, const GemmMaps& m, int grid, cudaStrea
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (g.pair)
+    return launch_pdl_cluster(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>, dim3(grid),
+                              dim3(threads_for(kFP8, kMX, kStage, kSplit)), kSmemBytes, s, 2, m.a, m.b, m.out, m.wsf,
+                              g);
   return launch_pdl(grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, kSplit>, dim3(grid),
                     dim3(threads_for(kFP8, kMX, kStage, kSplit)), kSmemBytes, s, m.a, m.b, m.out, m.wsf, g);
+}
+
+// Co-resident two-CTA clusters of one (unsplit) kernel variant, x 2.
+template <bool kFP8, bool kMX, int kStage, bool kFP4>
+int pair_ctas_one() {
+  static int cached = -1;
+  if (cached >= 0) return cached;
+  auto kernel = grouped_gemm_kernel<kFP8, kMX, kStage, kFP4, false>;
+  constexpr int kSmemBytes = Lay::kSmemBytes;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) return 0;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(threads_for(kFP8, kMX, kStage, false));
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    clusters = 0;
+  }
+  cached = 2 * clusters;
+  return cached;
+}
+
+template <bool kFP8, bool kMX, bool kFP4>
+int pair_ctas_stage(int stage) {
+  return stage == 1 ? pair_ctas_one<kFP8, kMX, 1, kFP4>() : pair_ctas_one<kFP8, kMX, 2, kFP4>();
 }
 
 template <bool kFP8, bool kMX, bool kFP4, bool kSplit>
@@ -806,6 +874,13 @@ __global__ void selftest_wait_kernel(int32_t* status, uint64_t timeout_ns) {
 
 cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& m, int grid, cudaStream_t s) {
   return g.k_splits > 1 ? launch_dtype<true>(g, m, grid, s) : launch_dtype<false>(g, m, grid, s);
+}
+
+int gemm_pair_ctas(const GemmArgs& g) {
+  if (g.fp4) return pair_ctas_stage<true, true, true>(g.stage);
+  if (g.mx) return pair_ctas_stage<true, true, false>(g.stage);
+  if (g.fp8) return pair_ctas_stage<true, false, false>(g.stage);
+  return pair_ctas_stage<false, false, false>(g.stage);
 }
 
 cudaError_t launch_selftest_wait(int32_t* status, uint64_t timeout_ns, cudaStream_t s) {

@@ -29,6 +29,27 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// launch_pdl for a kernel launched in clusters of cluster_x CTAs.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               int cluster_x, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 constexpr int kPlanChunk = 256;   // assignments per plan CTA (8 warps x 32)
 constexpr int kMaxLocalExperts = 1024;
 constexpr int kMaxTopk = 64;
@@ -122,6 +143,11 @@ struct GemmArgs {
   float* partial;             // [k_splits][part_rows][part_cols]
   int64_t part_rows;
   int64_t part_cols;          // n_blocks * 256
+  // Column-block pairs (compact layout, no split, even n_blocks): launched in
+  // clusters of two CTAs that always hold the same row block's column blocks
+  // 2m and 2m + 1; each CTA loads one 64-row half of the shared A tile and
+  // multicasts it to both.  The A map's box is then 64 rows.
+  int32_t pair;
 };
 
 // Problems the one-CTA plan handles: at most kPlanSmallMaxA assignments and
@@ -135,13 +161,17 @@ cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
 // Tensor maps of one grouped-GEMM launch.
 struct GemmMaps {
-  CUtensorMap a;     // A rows (a or h)
+  CUtensorMap a;     // A rows (a or h); 64-row boxes when g.pair
   CUtensorMap b;     // weights: w13 as [E][gate, up][I/128][128][K] (one box = a tile's gate and up
                      // rows), w2 as [E][K][I] in 256-row boxes
   CUtensorMap out;   // GEMM2: y, 32-column store boxes
   CUtensorMap wsf;   // MXFP8 / MXFP4: packed weight-scale chunks, a tile's two chunks per box
 };
 cudaError_t launch_gemm(const GemmArgs& g, const GemmMaps& maps, int grid, cudaStream_t s);
+// CTAs of a pair launch (g.pair) that can be resident at once: twice the
+// device's co-resident two-CTA clusters of the kernel g selects (0 when the
+// query fails).
+int gemm_pair_ctas(const GemmArgs& g);
 // After a split-K GEMM launch: adds each valid row's segment sums in segment
 // order and writes h (stage 1: SiLU*up, then FP8 / MXFP8 / bf16 storage) or y
 // (stage 2: bf16).  max_tiles: the static bound on the launch's tiles.
