@@ -773,7 +773,11 @@ def run_router(args, w, local):
     sec = ms / 1000.0
     flops = 2.0 * T * K * E
     segs = (K + 1023) // 1024
-    nbytes = 6.0 * E * K + 2.0 * T * K + 4.0 * T * E * (2 * segs + 1) + 8.0 * T * k
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fold = ((T + 127) // 128) * ((E + 127) // 128) * 4 >= sms * 3
+    # segment sums written and read back (small batches), or the logits
+    # written, read and rewritten by the top-k kernel (folded tiles)
+    nbytes = 6.0 * E * K + 2.0 * T * K + 4.0 * T * E * (3 if fold else 2 * segs + 1) + 8.0 * T * k
     peaks = load_peaks()
     t_tc = 3.0 * flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)

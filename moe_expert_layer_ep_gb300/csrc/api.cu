@@ -616,10 +616,12 @@ moe_status_t moe_route(const void* x_bf16, const void* w_planes, int64_t T, int6
   r.segs = static_cast<int32_t>((K + moe::kRouterSegment - 1) / moe::kRouterSegment);
   r.m_tiles = static_cast<int32_t>((T + 127) / 128);
   r.n_tiles = (E_global + 127) / 128;
+  r.fold = moe::router_folds(T, E_global, sms) ? 1 : 0;
   r.status = static_cast<int32_t*>(ws);
-  r.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  r.partial = r.fold ? nullptr : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
+  r.z = logits;
   r.timeout_ns = 2000000000ull;
-  const int64_t items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * r.segs;
+  const int64_t items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * (r.fold ? 1 : r.segs);
   const int grid = static_cast<int>(items < sms ? items : sms);
   return cuda_status(moe::launch_route(map_x, map_w, r, grid, topk, logits, topk_ids, topk_weights,
                                        static_cast<cudaStream_t>(stream)));

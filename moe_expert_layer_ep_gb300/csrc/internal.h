@@ -55,7 +55,7 @@ constexpr int kMaxLocalExperts = 1024;
 constexpr int kMaxTopk = 64;
 constexpr int kBlockM = 128;      // rows per expert block == compact block_e
 constexpr int kMaxRouterExperts = 1024;
-constexpr int kRouterSegment = 1024;     // K elements per router partial sum (fixed, batch-independent)
+constexpr int kRouterSegment = 1024;     // K elements per router segment sum (fixed, batch-independent)
 constexpr int kMaxKSplits = 8;           // K segments of a masked-layout GEMM tile, at most
 
 struct PlanArgs {
@@ -185,10 +185,20 @@ struct RouterArgs {
   int32_t E;
   int32_t segs;             // ceil(K / kRouterSegment)
   int32_t m_tiles, n_tiles; // ceil(T / 128), ceil(E / 128)
-  float* partial;           // [segs, T, E] fp32
+  int32_t fold;             // 1: one work item per tile, its segments added in the CTA
+  float* partial;           // fold == 0: [segs, T, E] fp32 segment sums
+  float* z;                 // fold == 1: the logits [T, E]
   int32_t* status;          // int32[4], cleared by the launch
   uint64_t timeout_ns;
 };
+// Router work items: when the 128 x 128 tiles fill at least three quarters of
+// the SMs, a CTA takes a whole tile and adds its segments itself (the
+// partial buffer goes unused); with fewer tiles, every segment of every tile
+// is its own item, for parallelism.  Either way the same segment sums are
+// added in the same order.
+inline bool router_folds(int64_t T, int64_t E, int sms) {
+  return ((T + 127) / 128) * ((E + 127) / 128) * 4 >= static_cast<int64_t>(sms) * 3;
+}
 
 cudaError_t launch_router_split(const float* w, uint16_t* planes, int64_t E, int64_t K, cudaStream_t s);
 cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, const RouterArgs& r, int grid, int topk,

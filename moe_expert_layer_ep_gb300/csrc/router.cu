@@ -12,15 +12,25 @@
 // (router_split_kernel); x is bf16, so each product x * plane is exact in the
 // fp32 accumulator and z = x.hi + x.mid + x.lo is the fp32-accumulated fp32
 // product.
-//   router_logits_tc_kernel  persistent, TMA-fed tcgen05 kernel over work
-//                            items (128 tokens x 128 experts x one 1024-wide K
-//                            segment); 12 bf16 MMAs per 64-wide K block into a
-//                            TMEM accumulator; fp32 partials per segment.
+//   router_logits_tc_kernel  persistent, TMA-fed tcgen05 kernel over 128-token
+//                            x 128-expert tiles; each tile's K runs in fixed
+//                            1024-wide segments, 12 bf16 MMAs per 64-wide K
+//                            block into a TMEM accumulator per segment, and
+//                            the logits are the segment sums added in order,
+//                            z = ((P0 + P1) + P2) + ... in fp32.  Work items:
+//                            fewer tiles than about the SMs (small batches):
+//                            one segment of one tile, the segment sums going
+//                            to a partial buffer for the top-k kernel to add;
+//                            more: a whole tile, its segments added in
+//                            registers as they complete and z written
+//                            directly.  The same operations in the same order
+//                            either way.
 //   topk_softmax_kernel      one warp per token: folds the partials in
-//                            segment order into the logits, then k rounds of
-//                            a warp argmax (larger logit wins, equal logits go
-//                            to the lower expert id), then
-//                            w_j = exp(z_j - z_max) / sum, the sum in j order.
+//                            segment order into the logits (or reads them),
+//                            then k rounds of a warp argmax (larger logit
+//                            wins, equal logits go to the lower expert id),
+//                            then w_j = exp(z_j - z_max) / sum, the sum in j
+//                            order.
 // Tiles, segments and the fold order do not depend on the batch, so a
 // token's logits, ids and weights are the same bits at every batch size.
 #include "common.cuh"
@@ -46,33 +56,46 @@ constexpr int kRtOffHolder = kRtOffBar + kRtNumBars * 8;
 constexpr int kRtOffAbort = kRtOffHolder + 8;
 constexpr int kRtSmemBytes = kRtOffAbort + 8 + 1024;      // + 1024-byte alignment slack
 constexpr uint32_t kRtTmemCols = 2 * kRtTileN;             // two accumulators
-constexpr int kRtThreads = 64 + 128;                       // producer, MMA, 4 epilogue warps
+constexpr int kRtEpiWarps = 8;                             // two per lane quadrant, 64 columns each
+constexpr int kRtThreads = 64 + 32 * kRtEpiWarps;          // producer, MMA, epilogue warps
 constexpr uint32_t kRtIdesc = (1u << 4)                    // D f32
                               | (1u << 7) | (1u << 10)     // A, B bf16
                               | (static_cast<uint32_t>(kRtTileN >> 3) << 17) |
                               (static_cast<uint32_t>(kRtTileM >> 4) << 24);
 static_assert(kRtSmemBytes <= 227 * 1024, "shared memory");
 
+// A work item: tile (mt, nt) and its segments [seg0, seg1) -- one segment
+// when the partials go to memory, all of them when the tile is folded in
+// the CTA (r.fold).
 struct RtItem {
-  int mt, nt, seg, kb0, nkb;
+  int mt, nt, seg0, seg1;
 };
 
 __device__ __forceinline__ RtItem rt_item(const RouterArgs& r, int64_t i) {
   RtItem it;
-  it.seg = static_cast<int>(i % r.segs);
-  it.nt = static_cast<int>((i / r.segs) % r.n_tiles);
-  it.mt = static_cast<int>(i / (static_cast<int64_t>(r.segs) * r.n_tiles));
-  it.kb0 = it.seg * (kRouterSegment / kRtKBlock);
-  const int kbs = static_cast<int>(r.K / kRtKBlock);
-  it.nkb = min(kRouterSegment / kRtKBlock, kbs - it.kb0);
+  const int per = r.fold ? 1 : r.segs;   // items per tile
+  it.seg0 = r.fold ? 0 : static_cast<int>(i % per);
+  it.seg1 = r.fold ? r.segs : it.seg0 + 1;
+  const int64_t tile = i / per;
+  it.nt = static_cast<int>(tile % r.n_tiles);
+  it.mt = static_cast<int>(tile / r.n_tiles);
   return it;
 }
 
-// One work item: a 128-token x 128-expert tile of one K segment.  Per 64-wide
-// K block, 4 K-steps x 3 weight planes = 12 MMAs in the fixed order (step,
-// plane), all into one fp32 accumulator; the segment's partial logits go to
-// partial[seg][t][e].  A token's partials are the same operations whatever
-// the batch (tile rows are independent), so the folded logits are too.
+// K blocks [kb0, kb0 + nkb) of segment seg.
+__device__ __forceinline__ void seg_blocks(const RouterArgs& r, int seg, int* kb0, int* nkb) {
+  constexpr int kPerSeg = kRouterSegment / kRtKBlock;
+  *kb0 = seg * kPerSeg;
+  *nkb = min(kPerSeg, static_cast<int>(r.K / kRtKBlock) - *kb0);
+}
+
+// Per segment of a work item: per 64-wide K block, 4 K-steps x 3 weight
+// planes = 12 MMAs in the fixed order (step, plane), all into one fp32
+// accumulator (two accumulators alternate between consecutive segments).  The
+// segment's sums go to partial[seg][t][e], or (r.fold) are added to the
+// thread's running row of 128 logits.  A token's partials are the same
+// operations whatever the batch (tile rows are independent), and so are the
+// folded logits.
 __global__ void __launch_bounds__(kRtThreads, 1)
     router_logits_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                             const RouterArgs r) {
@@ -96,7 +119,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * kRtEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -116,7 +139,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   // may still be read by the previous call's top-k kernel
   pdl_wait();
   pdl_trigger();
-  const int64_t n_items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * r.segs;
+  const int64_t n_items = static_cast<int64_t>(r.m_tiles) * r.n_tiles * (r.fold ? 1 : r.segs);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -126,13 +149,17 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       bool ok = true;
       for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const RtItem it = rt_item(r, i);
-        for (int kb = 0; kb < it.nkb; ++kb) {
+        int kb0, nkb, kb_last, nkb_last;
+        seg_blocks(r, it.seg0, &kb0, &nkb);
+        seg_blocks(r, it.seg1 - 1, &kb_last, &nkb_last);
+        const int kb_end = kb_last + nkb_last;
+        for (int kb = kb0; kb < kb_end && ok; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, r.timeout_ns)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[stage], kRtABytes + kRtBBytes);
-          const int kc = (it.kb0 + kb) * kRtKBlock;
+          const int kc = kb * kRtKBlock;
           tma_load_3d(smem + kRtOffA + stage * kRtABytes, &map_x, &full[stage], kc, it.mt * kRtTileM, 0);
           for (int p = 0; p < kRtPlanes; ++p)
             tma_load_3d(smem + kRtOffB + stage * kRtBBytes + p * kRtBPlaneBytes, &map_w, &full[stage], kc,
@@ -160,8 +187,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       uint32_t phase = 0;
       int iter = 0;
       bool ok = true;
-      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++iter) {
+      for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const RtItem it = rt_item(r, i);
+        for (int seg = it.seg0; seg < it.seg1 && ok; ++seg, ++iter) {
         const int acc = iter & 1;
         if (!mbar_wait_bounded(&tempty[acc], ((iter >> 1) & 1) ^ 1, abort_flag, r.timeout_ns)) {
           ok = false;
@@ -169,7 +197,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kRtTileN);
-        for (int kb = 0; kb < it.nkb; ++kb) {
+        int kb0, nkb;
+        seg_blocks(r, seg, &kb0, &nkb);
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort_flag, r.timeout_ns)) {
             ok = false;
             break;
@@ -192,6 +222,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         }
         if (!ok) break;
         tc_commit(&tfull[acc]);
+        }
       }
       if (!ok) {
         set_status(r.status, MOE_ERR_TIMEOUT);
@@ -202,43 +233,89 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       mbar_wait_bounded(done, 0, &never, r.timeout_ns);
     }
   } else {
-    const int quad = warp & 3;   // tensor-memory lane quadrant this warp may read
+    const int quad = warp & 3;            // tensor-memory lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;     // columns [64 half, 64 half + 64) of the tile
+    constexpr int kCols = kRtTileN / 2;
     int iter = 0;
-    for (int64_t i = blockIdx.x; i < n_items; i += gridDim.x, ++iter) {
+    bool failed = false;
+    for (int64_t i = blockIdx.x; i < n_items && !failed; i += gridDim.x) {
       const RtItem it = rt_item(r, i);
-      const int acc = iter & 1;
-      const bool got = mbar_wait_bounded(&tfull[acc], (iter >> 1) & 1, abort_flag, r.timeout_ns);
-      if (!__all_sync(0xFFFFFFFFu, got)) {
-        set_status(r.status, MOE_ERR_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
       const int64_t t = static_cast<int64_t>(it.mt) * kRtTileM + quad * 32 + lane;
-      const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kRtTileN) + (static_cast<uint32_t>(quad * 32) << 16);
-      float* dst = r.partial + (static_cast<int64_t>(it.seg) * r.T + t) * r.E;
-#pragma unroll 1
-      for (int c = 0; c < kRtTileN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, v);
-        tmem_ld_wait();
-        if (c == kRtTileN / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(&tempty[acc]);
+      float run[kCols];   // r.fold: this row's logits so far in this warp's columns, ((P0 + P1) + ...)
+      for (int seg = it.seg0; seg < it.seg1; ++seg, ++iter) {
+        const int acc = iter & 1;
+        const bool got = mbar_wait_bounded(&tfull[acc], (iter >> 1) & 1, abort_flag, r.timeout_ns);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+          set_status(r.status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+          failed = true;
+          break;
         }
-        const int e0 = it.nt * kRtTileN + c * 32;
-        if (t < r.T && e0 < r.E) {
-          if (e0 + 32 <= r.E && (r.E & 3) == 0) {
-            float4* d4 = reinterpret_cast<float4*>(dst + e0);
+        tc_fence_after();
+        const uint32_t taddr = tmem + static_cast<uint32_t>(acc * kRtTileN + half * kCols) +
+                               (static_cast<uint32_t>(quad * 32) << 16);
+        if (r.fold) {
+          const bool first = seg == it.seg0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-          } else {
+          for (int c = 0; c < kCols / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, v);
+            tmem_ld_wait();
+            if (c == kCols / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(&tempty[acc]);
+            }
+            if (first) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (e0 + j < r.E) dst[e0 + j] = __uint_as_float(v[j]);
+              for (int j = 0; j < 32; ++j) run[c * 32 + j] = __uint_as_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) run[c * 32 + j] += __uint_as_float(v[j]);
+            }
           }
+          continue;
+        }
+        float* dst = r.partial + (static_cast<int64_t>(seg) * r.T + t) * r.E;
+#pragma unroll 1
+        for (int c = 0; c < kCols / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, v);
+          tmem_ld_wait();
+          if (c == kCols / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&tempty[acc]);
+          }
+          const int e0 = it.nt * kRtTileN + half * kCols + c * 32;
+          if (t < r.T && e0 < r.E) {
+            if (e0 + 32 <= r.E && (r.E & 3) == 0) {
+              float4* d4 = reinterpret_cast<float4*>(dst + e0);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                    __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (e0 + j < r.E) dst[e0 + j] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+      if (failed || !r.fold || t >= r.T) continue;
+      float* zrow = r.z + t * r.E;
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) {
+        const int e0 = it.nt * kRtTileN + half * kCols + c * 32;
+        if (e0 + 32 <= r.E && (r.E & 3) == 0) {
+          float4* d4 = reinterpret_cast<float4*>(zrow + e0);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            d4[j] = make_float4(run[c * 32 + 4 * j], run[c * 32 + 4 * j + 1], run[c * 32 + 4 * j + 2],
+                                run[c * 32 + 4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (e0 + j < r.E) zrow[e0 + j] = run[c * 32 + j];
         }
       }
     }
@@ -290,18 +367,33 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* partial,
   pdl_trigger();
   if (t >= T) return;
   float v[P];
-  // logits = the segments' partial sums folded in segment order
+  // logits = the segments' partial sums folded in segment order; the loads
+  // of kBatch segments are all issued before any of them is added
+  constexpr int kBatch = P >= 32 ? 1 : 32 / P;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     const int e = lane + 32 * i;
-    if (e < E) {
-      float acc = partial[t * E + e];
-      for (int sg = 1; sg < segs; ++sg) acc += partial[(static_cast<int64_t>(sg) * T + t) * E + e];
-      v[i] = acc;
-      z[t * E + e] = acc;
-    } else {
-      v[i] = -INFINITY;
-    }
+    v[i] = e < E ? partial[t * E + e] : -INFINITY;
+  }
+  for (int sg = 1; sg < segs; sg += kBatch) {
+    float p[kBatch][P];
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q)
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        const int e = lane + 32 * i;
+        p[q][i] = (sg + q < segs && e < E) ? partial[(static_cast<int64_t>(sg + q) * T + t) * E + e] : 0.0f;
+      }
+#pragma unroll
+    for (int q = 0; q < kBatch; ++q)
+#pragma unroll
+      for (int i = 0; i < P; ++i)
+        if (sg + q < segs && lane + 32 * i < E) v[i] += p[q][i];
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) z[t * E + e] = v[i];
   }
   uint32_t taken = 0;      // bit i: element lane + 32 i already selected
   float my_v0 = 0.0f, my_v1 = 0.0f;
@@ -378,10 +470,11 @@ cudaError_t launch_route(const CUtensorMap& map_x, const CUtensorMap& map_w, con
   if (e != cudaSuccess) return e;
   const int warps = 8;
   const dim3 nb(static_cast<unsigned>((r.T + warps - 1) / warps)), block(warps * 32);
-  const int segs = r.segs;
+  // folded logits were written by the logits kernel: read back as one segment
+  const int segs = r.fold ? 1 : r.segs;
   const int E = r.E;
   const int64_t T = r.T;
-  const float* partial = r.partial;
+  const float* partial = r.fold ? r.z : r.partial;
   if (r.E <= 128) return launch_pdl(topk_softmax_kernel<4>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
   if (r.E <= 256) return launch_pdl(topk_softmax_kernel<8>, nb, block, 0, s, partial, segs, T, E, topk, logits, ids, wts);
   if (r.E <= 512)

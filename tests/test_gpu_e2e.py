@@ -116,6 +116,44 @@ def test_repeat_runs_bitwise_and_graph_replay(case):
     assert not torch.equal(g.out.view(torch.int16), first.view(torch.int16))
 
 
+_FIRST_CALL_CAPTURED = r"""
+import sys
+import torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + "/tests"]
+from moe_testlib import Problem
+p = Problem(T=257, K=512, I=256, E_global=16, E_local=16, topk=4, dtype=sys.argv[2], layout="compact", seed=3)
+g = p.gpu()
+s = torch.cuda.Stream()
+s.wait_stream(torch.cuda.current_stream())
+graph = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph, stream=s):
+    g.forward()
+graph.replay()
+torch.cuda.synchronize()
+captured = g.out.clone()
+g.out.zero_()
+eager = g.forward().clone()
+torch.cuda.synchronize()
+assert g.status() == 0
+assert torch.equal(captured.view(torch.int16), eager.view(torch.int16))
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("dtype", ["fp8", "bf16"])
+def test_first_forward_of_a_process_inside_graph_capture(dtype):
+    """The library sets kernel attributes and queries cluster residency on a
+    kernel's first use; a process whose first forward is being captured into
+    a CUDA graph must still capture and replay it (FP8: the paired GEMMs)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_CAPTURED, root, dtype], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
 def _sampled_check(p, g, tokens):
     out = bf16_to_f64(g.forward())
     assert g.status() == 0

@@ -9,7 +9,8 @@ logits (the comparison that decides an id is taken in the kernel's
 precision), including rows with tied logits.  Weights: the oracle's softmax
 of the same logits, within a few fp32 ulps.  Batch invariance: a token's
 outputs do not depend on the batch around it, whichever kernel its batch
-size selects.
+size selects: a large batch adds each tile's K segments inside the logits
+kernel, a small one through a partial buffer, in the same order.
 """
 
 import numpy as np
@@ -96,6 +97,20 @@ def test_router_logits_identical_across_batch_sizes():
         part = [t.cpu() for t in M.moe_route(x[:n].cuda(), wc, 6)]
         for a, b in zip(part, full):
             assert torch.equal(a, b[:n])
+
+
+def test_router_folded_and_partial_paths_agree_bitwise():
+    """A batch whose 128 x 128 tiles fill most of the GPU is folded inside
+    the logits kernel, a smaller one through the partial buffer: the same
+    tokens get the same bits either way (K = 1152 ends in a short segment)."""
+    x, w = _inputs(2048, 1152, 1024, 21)      # 16 x 8 = 128 tiles
+    wc = _planes(w)
+    big = [t.cpu() for t in M.moe_route(x.cuda(), wc, 8)]
+    rows = [0, 5, 517, 2047]
+    small = [t.cpu() for t in M.moe_route(x[rows].cuda(), wc, 8)]
+    for a, b in zip(small, big):
+        assert torch.equal(a, b[rows])
+    _check(x[:200], w, 8)
 
 
 def test_router_weight_split_is_exact():
