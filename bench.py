@@ -236,8 +236,12 @@ def work_model(w, ids):
     g1_bytes = w13_bytes + a_bytes + h_bytes
     g2_bytes = w2_bytes + h_bytes + y_bytes
     route = T * k * 8
+    # the memory-bound passes: quant-scatter reads x and the routing and
+    # writes the a rows; combine reads the y rows and the routing and writes out
+    quant = (T * K * 2 + T * k * 4, a_bytes)
+    combine = (y_bytes + route, T * K * 2)
     return {"A": A, "nonempty": nonempty, "flops1": flops1, "flops2": flops2, "g1_bytes": g1_bytes,
-            "g2_bytes": g2_bytes, "weights_bytes": w13_bytes + w2_bytes,
+            "g2_bytes": g2_bytes, "weights_bytes": w13_bytes + w2_bytes, "quant_rw": quant, "combine_rw": combine,
             "fused_bytes": w13_bytes + w2_bytes + 2 * T * K * 2 + route,
             "layer_bytes": w13_bytes + w2_bytes + 2 * T * K * 2 + route + 2 * (a_bytes + h_bytes + y_bytes)}
 
@@ -407,6 +411,37 @@ def gemm_roofline(name, flops, nbytes, ms, peaks, fp8):
     return roof
 
 
+def measure_write_peak(dev):
+    """Write-only HBM bandwidth of this GPU: torch's fill of a 512 MB buffer,
+    CUDA events over 10 fills after 3 untimed ones.  A stream of writes
+    alone runs well below the copy bandwidth (a read and a write per byte)
+    the roofline peaks are measured with."""
+    buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        buf.fill_(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(10):
+        buf.fill_(i)
+    e1.record()
+    torch.cuda.synchronize()
+    gbs = 10 * buf.numel() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del buf
+    return gbs
+
+
+def memory_pass(ms, rw, peaks, write_gbs):
+    """An HBM-bound pass: achieved GB/s against the copy bandwidth, and its
+    time against the time its writes alone take at the write-only bandwidth."""
+    rd, wr = rw
+    sec = ms / 1000.0
+    gbs = (rd + wr) / sec / 1e9
+    write_ms = wr / (write_gbs * 1e9) * 1000.0
+    return {"ms": round(ms, 4), "read_bytes": int(rd), "write_bytes": int(wr), "achieved_gbs": round(gbs, 1),
+            "frac_of_copy_peak": round(gbs / peaks["hbm_gbs"], 4), "writes_alone_ms": round(write_ms, 4),
+            "frac_of_write_bound": round(write_ms / ms, 4)}
+
+
 def pct(a, q):
     return round(float(np.percentile(np.asarray(a), q)), 4)
 
@@ -537,6 +572,7 @@ def run_ours(args, w, world, rank, local):
     step_ms = [step_ev[s].elapsed_time(step_ev[s + 1]) for s in range(args.steps)]
     stage_ms = np.array([[stage_ev[s][i].elapsed_time(stage_ev[s][i + 1]) for i in range(nst)]
                          for s in range(args.steps)])
+    write_gbs = measure_write_peak(dev)
 
     # end to end through the C-ABI with host buffers, as a serving loop runs
     # it: every step copies its x / ids / weights from pinned host memory and
@@ -650,6 +686,10 @@ def run_ours(args, w, world, rank, local):
                                 "frac": round(fused_ms / ms_per_step, 4),
                                 "what": "weights of non-empty experts + x + out (+ routing) at the measured "
                                         "HBM bandwidth, or the tensor time if larger"},
+        "memory_passes": {"write_peak_gbs": round(write_gbs, 1),
+                          "write_peak_how": "torch fill of 512 MB, measured in this run",
+                          "quant_scatter": memory_pass(float(med[1]), wm["quant_rw"], peaks, write_gbs),
+                          "combine": memory_pass(float(med[4]), wm["combine_rw"], peaks, write_gbs)},
         "stage_ms": {n: round(float(v), 4) for n, v in zip(names, med)},
         "stage_ms_p10": {n: pct(stage_ms[:, i], 10) for i, n in enumerate(names)},
         "stage_ms_p90": {n: pct(stage_ms[:, i], 90) for i, n in enumerate(names)},
