@@ -111,8 +111,9 @@ typedef struct {
   uint64_t chunk_hist;  /* int32[E_local * chunks] plan scratch */
   uint64_t chunk_rank;  /* int32[T * topk]         plan scratch */
   uint64_t a;           /* [rows, K]  fp8 bytes or bf16: expert inputs */
-  uint64_t a_sf;        /* fp8 / mxfp8: scale chunks of a (see moe_sf_offset); MXFP8 stores the four
-                           32-column scales of a row and 128-column group in the word's four bytes */
+  uint64_t a_sf;        /* fp8 / mxfp8: scale chunks of a (see moe_sf_offset); FP8 stores four consecutive
+                           128-column groups' scales of a row in one word's four bytes, MXFP8 the four
+                           32-column scales of a row and 128-column group */
   uint64_t h;           /* [rows, I]  fp8 bytes or bf16: silu(gate) * up */
   uint64_t h_sf;        /* fp8 / mxfp8: scale chunks of h */
   uint64_t y;           /* [rows, K]  bf16: expert outputs */
@@ -320,11 +321,13 @@ moe_status_t moe_clear_device_status(void* ws, void* stream);
  * normally, leaving the context usable.  Enqueued on stream. */
 moe_status_t moe_selftest_wait_timeout(void* ws, int64_t timeout_ns, void* stream);
 
-/* Byte offset, inside a scale region (a_sf or h_sf), of the UE8M0 byte for
- * (row block b, 128-column group g, row r in 0..127) when a row block holds
- * n_groups groups.  Each (block, group) chunk is 512 bytes laid out for the
- * tensor-memory scale copy: byte 16*(r%32) + 4*(r/32) + c, c = 0..3 (the
- * four copies are equal).  Host helper for tests. */
+/* Byte offset, inside an FP8 (1x128) scale region (a_sf or h_sf), of the
+ * UE8M0 byte for (row block b, 128-column group g, row r in 0..127) when a
+ * row block holds n_groups groups.  Each (block, four consecutive groups)
+ * chunk is 512 bytes laid out for the tensor-memory scale copy: row r's word
+ * at byte 16*(r%32) + 4*(r/32), group g's scale in its byte g % 4, so that
+ * one copy serves the MMAs of four K blocks.  (MXFP8: one chunk per group,
+ * the word's bytes its four 32-column scales.)  Host helper for tests. */
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row);
 
 const char* moe_strerror(moe_status_t status);

@@ -640,7 +640,7 @@ moe_status_t moe_pack_mx_scales(const uint8_t* src, int64_t src_ld, uint8_t* dst
 }
 
 int64_t moe_sf_offset(int64_t block, int64_t group, int64_t n_groups, int32_t row) {
-  return moe::sf_chunk_offset(block, group, n_groups) + moe::sf_row_offset(row);
+  return moe::sf_fp8_offset(block, group, n_groups, row);
 }
 
 const char* moe_strerror(moe_status_t s) {

@@ -324,13 +324,23 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
-// Scale chunk layout: one 512-byte chunk per (128-row block, 128-column
-// group); row r's byte sits at 16 * (r % 32) + 4 * (r / 32), repeated four
-// times (the tensor-memory scale copy reads 32 rows x 16 bytes and places row
-// 32 * i + j's scale in column i of lane j).
-__host__ __device__ __forceinline__ int64_t sf_chunk_offset(int64_t block, int64_t group, int64_t n_groups) {
-  return (block * n_groups + group) * 512;
+// Scale chunk layout: 512-byte chunks, row r's 32-bit word of a chunk at
+// byte 16 * (r % 32) + 4 * (r / 32) (the tensor-memory scale copy reads 32
+// rows x 16 bytes and places row 32 * i + j's word in column i of lane j).
+// The MMA reads byte ID (0..3) of a row's word, chosen per MMA.
+//   MXFP8: one chunk per (128-row block, 128-column group); the word's four
+//          bytes are the group's four 32-column scales.
+//   FP8 1x128: one chunk per (128-row block, four consecutive 128-column
+//          groups 4q .. 4q + 3); the word's byte j is group 4q + j's scale,
+//          so one copy into tensor memory serves four K blocks.
+__host__ __device__ __forceinline__ int64_t sf_chunk_offset(int64_t block, int64_t chunk, int64_t n_chunks) {
+  return (block * n_chunks + chunk) * 512;
 }
 __host__ __device__ __forceinline__ int sf_row_offset(int r) { return 16 * (r & 31) + 4 * (r >> 5); }
+__host__ __device__ __forceinline__ int64_t sf_quads(int64_t n_groups) { return (n_groups + 3) >> 2; }
+// FP8 1x128: the byte of (row block, 128-column group, row).
+__host__ __device__ __forceinline__ int64_t sf_fp8_offset(int64_t block, int64_t group, int64_t n_groups, int r) {
+  return sf_chunk_offset(block, group >> 2, sf_quads(n_groups)) + sf_row_offset(r) + (group & 3);
+}
 
 }  // namespace moe

@@ -289,7 +289,11 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
       tile_b_rows<kStage>(g, tl, &r0, &r1);
       const int a_e = g.masked ? tl.expert : 0;
       const int kb_end = seg_begin(seg + 1, S, k_blocks);
-      for (int kb = seg_begin(seg, S, k_blocks); kb < kb_end; ++kb) {
+      const int kb_begin = seg_begin(seg, S, k_blocks);
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        // FP8 1x128: the activation scales of K blocks 4q .. 4q + 3 arrive
+        // with the stage of the unit's first K block of quad q
+        const bool sfa_new = kFP8 && (kMX || (kb & 3) == 0 || kb == kb_begin);
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, g.timeout_ns);
         w_ok = __shfl_sync(0xFFFFFFFFu, w_ok, 0);
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
         }
         if (lane == 0) {
           const uint32_t bytes =
-              kABytes + (kFP4 ? kBPBytes : kBBytes) + (kFP8 ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
+              kABytes + (kFP4 ? kBPBytes : kBBytes) + (sfa_new ? kSfaBytes : 0) + (kMX ? kSfbBytes : 0);
           // (FP4: the unpacking copy leaves the 8-byte gaps of each 16-byte
           // group unwritten and counts only the 16 KB of codes)
           mbar_arrive_expect_tx(&full[stage], bytes);
@@ -316,9 +320,10 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
             tma_load_5d(bdst, &map_b, &full[stage], kc, 0, tl.nb, 0, tl.expert);
           else
             tma_load_3d(bdst, &map_b, &full[stage], kc, r0, tl.expert);
-          if (kFP8) {
-            bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + sf_chunk_offset(tl.sf_block, kb, k_blocks),
-                      kSfaBytes, &full[stage]);
+          if (sfa_new) {
+            const int64_t chunk = kMX ? sf_chunk_offset(tl.sf_block, kb, k_blocks)
+                                      : sf_chunk_offset(tl.sf_block, kb >> 2, sf_quads(k_blocks));
+            bulk_load(smem + kOffSfa + stage * kSfaBytes, g.a_sf + chunk, kSfaBytes, &full[stage]);
           }
           if (kMX) {
             // B scale tile: the packed 512-byte chunks of the tile's two
@@ -358,6 +363,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
       int stage = 0;
       uint32_t phase = 0;
       int iter = 0;
+      int sf_stage = 0;   // FP8 1x128: the stage whose scale slot holds the current quad's scales
       bool ok = true;
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++iter) {
         const int seg = static_cast<int>(u % S);
@@ -382,19 +388,26 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
           const uint64_t a_desc = smem_desc(a_addr, 16, 1024, kSwizzle128B);
           const uint64_t b_desc = smem_desc(b_addr, 16, 1024, kSwizzle128B);
           if (kFP8) {
-            const uint32_t sfa_t = tmem + kSfTmemCol + 32u * stage;
+            // scale tiles into tensor memory: every K block (MX), or once per
+            // quad of K blocks (1x128: byte kb % 4 of each row's word)
+            if (kMX || (kb & 3) == 0 || first) {
+              const uint32_t sfa_t = tmem + kSfTmemCol + 32u * stage;
+              const uint32_t sfb_t = sfa_t + 16u;
+              const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
+              const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
+              tmem_cp_32x128b_x4(sfa_t, smem_desc(sfa_s, 16, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4(sfb_t, smem_desc(sfb_s, 16, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4(sfb_t + 4u, smem_desc(sfb_s + 512u, 16, 128, kSwizzleNone));
+              sf_stage = stage;
+            }
+            const uint32_t sfa_t = tmem + kSfTmemCol + 32u * sf_stage;
             const uint32_t sfb_t = sfa_t + 16u;
-            const uint32_t sfa_s = smem_u32(smem + kOffSfa + stage * kSfaBytes);
-            const uint32_t sfb_s = smem_u32(smem + kOffSfb + stage * kSfbBytes);
-            tmem_cp_32x128b_x4(sfa_t, smem_desc(sfa_s, 16, 128, kSwizzleNone));
-            tmem_cp_32x128b_x4(sfb_t, smem_desc(sfb_s, 16, 128, kSwizzleNone));
-            tmem_cp_32x128b_x4(sfb_t + 4u, smem_desc(sfb_s + 512u, 16, 128, kSwizzleNone));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k,
-                                   kMX ? (kIdescB | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4))
-                                       : kIdescB,
-                                   sfa_t, sfb_t, !(first && k == 0));
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t id = kMX ? static_cast<uint32_t>(k) : static_cast<uint32_t>(kb & 3);
+              mma_fp8_block_scaled(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdescB | (id << 29) | (id << 4), sfa_t,
+                                   sfb_t, !(first && k == 0));
+            }
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -423,15 +436,26 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
     }
   } else if (scale_warps(kFP8, kMX) && warp == 2 + epi_warps(kFP8, kStage, kSplit)) {
     // ------------------------------------------------------------------ weight-scale tiles (FP8)
-    // B scale tile of each stage: 256 rows, rows 0..127 share the first
-    // weight block's scale, rows 128..255 the second's; 1 KB written by the
-    // warp, then its arrival completes the stage with the producer's copies.
+    // B scale tile, written into the stage of a unit's first K block of each
+    // quad q of K blocks: 256 rows, rows 0..127 of the first weight row block
+    // and 128..255 of the second, each row's word holding the block's scales
+    // of K blocks 4q .. 4q + 3 (byte j: K block 4q + j); 1 KB written by the
+    // warp.  The warp arrives on every stage's barrier, beside the producer's
+    // copies.
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    // weight-scale rows of a unit's two weight row blocks, and the scales
-    // of its first 32 K blocks (one per lane); the next unit's are read
-    // while the current unit's tiles are written
+    // a weight row block's scales of K blocks 4q .. 4q + 3 as one word
+    auto quad_word = [&](int64_t base, int q) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (4 * q + j < k_blocks) w |= static_cast<uint32_t>(g.w_sf[base + 4 * q + j]) << (8 * j);
+      return w;
+    };
+    // weight-scale rows of a unit's two weight row blocks, and their words of
+    // the 32 quads from the unit's first (one per lane); the next unit's are
+    // read while the current unit's tiles are written
     auto unit_scales = [&](int64_t u, int64_t* base_sg, int64_t* base_su, uint32_t* sg, uint32_t* su) {
       const int64_t t = u / S;
       const int seg = static_cast<int>(u - t * S);
@@ -441,11 +465,9 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
       const int64_t base = static_cast<int64_t>(tl.expert) * g.w_rows_blocks;
       *base_sg = (base + min(r0 >> 7, g.w_rows_blocks - 1)) * g.w_k_groups;
       *base_su = (base + min(r1 >> 7, g.w_rows_blocks - 1)) * g.w_k_groups;
-      const int kk = seg_begin(seg, S, k_blocks) + lane;
-      if (kk < seg_begin(seg + 1, S, k_blocks)) {
-        *sg = g.w_sf[*base_sg + kk];
-        *su = g.w_sf[*base_su + kk];
-      }
+      const int q = (seg_begin(seg, S, k_blocks) >> 2) + lane;
+      *sg = quad_word(*base_sg, q);
+      *su = quad_word(*base_su, q);
     };
     int64_t nb_sg = 0, nb_su = 0;
     uint32_t n_sg = 0, n_su = 0;
@@ -457,14 +479,14 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
       uint32_t sg_cache = n_sg, su_cache = n_su;
       if (u + gridDim.x < n_units) unit_scales(u + gridDim.x, &nb_sg, &nb_su, &n_sg, &n_su);
       const int kb_begin = seg_begin(seg, S, k_blocks), kb_end = seg_begin(seg + 1, S, k_blocks);
+      int q0 = kb_begin >> 2;   // first quad of the lanes' words
       for (int kb = kb_begin; kb < kb_end; ++kb) {
-        if (kb > kb_begin && ((kb - kb_begin) & 31) == 0) {
-          // weight scales of the next 32 K blocks, one per lane
-          const int kk = kb + lane;
-          if (kk < kb_end) {
-            sg_cache = g.w_sf[base_sg + kk];
-            su_cache = g.w_sf[base_su + kk];
-          }
+        const int q = kb >> 2;
+        if (q - q0 == 32) {
+          // the next 32 quads, one per lane
+          q0 += 32;
+          sg_cache = quad_word(base_sg, q0 + lane);
+          su_cache = quad_word(base_su, q0 + lane);
         }
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, g.timeout_ns);
@@ -473,13 +495,15 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
           ok = false;
           break;
         }
-        const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, (kb - kb_begin) & 31);
-        const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, (kb - kb_begin) & 31);
-        const uint32_t word = (lane < 16 ? sg : su) * 0x01010101u;
-        uint4* dst = reinterpret_cast<uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane * 2;
-        dst[0] = make_uint4(word, word, word, word);
-        dst[1] = make_uint4(word, word, word, word);
-        fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor-memory copy
+        if ((kb & 3) == 0 || kb == kb_begin) {
+          const uint32_t sg = __shfl_sync(0xFFFFFFFFu, sg_cache, q - q0);
+          const uint32_t su = __shfl_sync(0xFFFFFFFFu, su_cache, q - q0);
+          const uint32_t word = lane < 16 ? sg : su;
+          uint4* dst = reinterpret_cast<uint4*>(smem + kOffSfb + stage * kSfbBytes) + lane * 2;
+          dst[0] = make_uint4(word, word, word, word);
+          dst[1] = make_uint4(word, word, word, word);
+          fence_proxy_async_smem();   // generic-proxy stores -> visible to the tensor-memory copy
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[stage]);
         if (++stage == kStages) {
@@ -664,10 +688,7 @@ __global__ void __launch_bounds__(threads_for(kFP8, kMX, kStage, kSplit), 1)
                     (cvt_e4m3x2(h[b + 14] * mul, h[b + 15] * mul) << 16);
               dst[v] = o;
             }
-            if (half == 0) {
-              *reinterpret_cast<uint32_t*>(g.out_sf + sf_chunk_offset(tl.sf_block, tl.nb, g.out_groups) +
-                                           sf_row_offset(r)) = static_cast<uint32_t>(s + 127) * 0x01010101u;
-            }
+            if (half == 0) g.out_sf[sf_fp8_offset(tl.sf_block, tl.nb, g.out_groups, r)] = static_cast<uint8_t>(s + 127);
           }
         } else if (row_ok) {
           uint4* dst =

@@ -78,7 +78,7 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& q, int64_t t,
 #pragma unroll
         for (int o = kMX ? 2 : 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         const int s = ue8m0_exponent(amax);
-        uint32_t sf_word = static_cast<uint32_t>(s + 127) * 0x01010101u;
+        uint32_t sf_word = static_cast<uint32_t>(s + 127);
         if constexpr (kMX) {
           const int lane = tid & 31;
           const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(s + 127), lane + 4);
@@ -99,8 +99,11 @@ __device__ __forceinline__ void quant_scatter_row(const QuantArgs& q, int64_t t,
             uint8_t* arow = static_cast<uint8_t*>(q.a) + d * q.K;
             *reinterpret_cast<uint2*>(arow + col) = packed;
             if (group_lead) {
-              *reinterpret_cast<uint32_t*>(q.a_sf + sf_chunk_offset(s_blk[j], group, n_groups) +
-                                           sf_row_offset(s_row[j])) = sf_word;
+              if (kMX)   // the group's four 32-column scales, one word
+                *reinterpret_cast<uint32_t*>(q.a_sf + sf_chunk_offset(s_blk[j], group, n_groups) +
+                                             sf_row_offset(s_row[j])) = sf_word;
+              else       // the group's byte of its four-group word
+                q.a_sf[sf_fp8_offset(s_blk[j], group, n_groups, s_row[j])] = static_cast<uint8_t>(sf_word);
             }
           }
         }

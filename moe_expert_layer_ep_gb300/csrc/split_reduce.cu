@@ -78,12 +78,12 @@ __global__ void __launch_bounds__(kRedThreads) split_reduce_act_kernel(const Gem
         const int e = ue8m0_exponent(amax);
         static_cast<uint8_t*>(g.out)[row * g.out_ld + col] =
             static_cast<uint8_t>(cvt_e4m3x2(h * exp2_neg(e), 0.0f) & 0xFFu);
-        uint8_t* sf = g.out_sf + sf_chunk_offset(sf_block, nb, g.out_groups) + sf_row_offset(r);
         if (kMX) {
           // byte k of the row's scale word: 32-column block k
+          uint8_t* sf = g.out_sf + sf_chunk_offset(sf_block, nb, g.out_groups) + sf_row_offset(r);
           if (lane == 0) sf[warp] = static_cast<uint8_t>(e + 127);
         } else if (c == 0) {
-          *reinterpret_cast<uint32_t*>(sf) = static_cast<uint32_t>(e + 127) * 0x01010101u;
+          g.out_sf[sf_fp8_offset(sf_block, nb, g.out_groups, r)] = static_cast<uint8_t>(e + 127);
         }
       } else {
         const __nv_bfloat16 v = __float2bfloat16_rn(h);

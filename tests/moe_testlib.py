@@ -182,9 +182,13 @@ class GpuLayer:
         else:
             blk, r = rows // 128, rows % 128
         g = np.arange(groups)
-        off = (blk[:, None] * groups + g[None, :]) * 512 + (16 * (r % 32) + 4 * (r // 32))[:, None]
-        if self.ctx.mx:
+        row_off = (16 * (r % 32) + 4 * (r // 32))[:, None]
+        if self.ctx.mx:   # one chunk per group, the word's bytes its four 32-column blocks
+            off = (blk[:, None] * groups + g[None, :]) * 512 + row_off
             return sf[(off[:, :, None] + np.arange(4)[None, None, :]).reshape(len(rows), 4 * groups)]
+        # FP8 1x128: one chunk per four groups, group g in byte g % 4 of the word
+        quads = -(-groups // 4)
+        off = (blk[:, None] * quads + g[None, :] // 4) * 512 + row_off + g[None, :] % 4
         return sf[off]
 
     def decoded(self, name, rows):

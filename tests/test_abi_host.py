@@ -41,9 +41,15 @@ def test_compact_bound_and_layout_choice_match_oracle():
 
 
 def test_scale_chunk_offsets_are_a_bijection():
-    offs = {M.moe_sf_offset(b, g, 3, r) for b in range(2) for g in range(3) for r in range(128)}
-    assert len(offs) == 2 * 3 * 128
-    assert all(o % 4 == 0 and 0 <= o < 2 * 3 * 512 for o in offs)
+    """FP8 1x128 scale bytes: four consecutive 128-column groups share a
+    512-byte chunk per row block, group g in byte g % 4 of the row's word."""
+    for n_groups in (3, 4, 5, 56):
+        quads = -(-n_groups // 4)
+        offs = [M.moe_sf_offset(b, g, n_groups, r) for b in range(2) for g in range(n_groups) for r in range(128)]
+        assert len(set(offs)) == len(offs) == 2 * n_groups * 128
+        assert all(0 <= o < 2 * quads * 512 for o in offs)
+        for b, g, r in ((1, n_groups - 1, 77), (0, 2, 31), (1, 0, 127)):
+            assert M.moe_sf_offset(b, g, n_groups, r) == (b * quads + g // 4) * 512 + 16 * (r % 32) + 4 * (r // 32) + g % 4
 
 
 def test_status_strings():

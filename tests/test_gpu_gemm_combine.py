@@ -175,12 +175,11 @@ def test_gemm2_block_scales_exact(layout, I):
     offs = []
     vals = []
     for gidx in range(I // 128):
-        offs.append((blk * (I // 128) + gidx) * 512 + 16 * (r_in % 32) + 4 * (r_in // 32))
+        offs.append(np.array([M.moe_sf_offset(int(b), gidx, I // 128, int(r)) for b, r in zip(blk, r_in)]))
         vals.append(r_in - 64 + 127)
     offs = np.concatenate(offs)
     vals = np.concatenate(vals).astype(np.uint8)
-    for c in range(4):
-        sf[torch.as_tensor(offs + c, device="cuda")] = torch.as_tensor(vals, device="cuda")
+    sf[torch.as_tensor(offs, device="cuda")] = torch.as_tensor(vals, device="cuda")
     g.gemm2()
     torch.cuda.synchronize()
     assert g.status() == 0
