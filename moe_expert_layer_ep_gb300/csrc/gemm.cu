@@ -12,8 +12,11 @@
 // standard MoE dispatch" (sglang PR #33128 report), "实现拆解" steps 1 and 3):
 // 1x128 per activation row and 128x128 per weight block.  Because the scales
 // are powers of two, they are handed to the block-scaled MMA
-// (kind::mxf8f6f4, one scale per 32 K-elements) by repeating each 1x128 scale
-// over its four 32-element sub-blocks: the products are the same, exactly.
+// (kind::mxf8f6f4, one scale per 32 K-elements) by giving all four 32-element
+// sub-blocks of a K block the same scale: the products are the same, exactly.
+// A row's scale word holds the scales of four consecutive K blocks, one per
+// byte, and the MMAs of K block kb read byte kb % 4 (scale-factor ID), so the
+// scale tiles are copied into tensor memory once per four K blocks.
 // The MXFP8 variant (1x32 scales everywhere; listed as uncovered in the
 // standard-dispatch report's "风险与影响" item 5) hands each 32-element
 // sub-block its own scale byte: the k-th MMA of a 128-byte K block reads byte
@@ -38,15 +41,17 @@
 // One persistent CTA per SM:
 //   warp 0      TMA producer: per K block the A tile, the whole B tile in one
 //               box (GEMM1's gate and up rows through a 5-d view of w13) and
-//               the activation scale chunk (+ both MX weight-scale chunks in
-//               one box).  TMA accepts about 130 bytes per cycle per SM, so
-//               the producer's loop does nothing else.
+//               the activation scale chunk (once per four K blocks for 1x128
+//               scales; + both MX weight-scale chunks in one box).  TMA
+//               accepts about 130 bytes per cycle per SM, so the producer's
+//               loop does nothing else.
 //   warp 1      TMEM allocation + single-thread MMA issue (tcgen05.cp of the
 //               scale tiles, 4 MMAs of K=32 bytes per 128-byte K block)
 //   epilogue    4 or 8 warps (see epi_warps): tcgen05.ld of the accumulator,
 //               then activation / quantisation and stores of valid rows
-//   scale warp  FP8 with 128x128 weight scales: expands each stage's weight
-//               scale tile in shared memory and arrives beside the producer
+//   scale warp  FP8 with 128x128 weight scales: writes each quad of K
+//               blocks' weight-scale tile in shared memory and arrives on
+//               every stage beside the producer
 // A 4-stage mbarrier ring connects producer and MMA; accumulator barriers
 // connect MMA and epilogue (two accumulators on the BF16 path, one on the FP8
 // path, whose other tensor-memory columns hold the scale tiles).
