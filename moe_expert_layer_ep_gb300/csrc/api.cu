@@ -402,14 +402,15 @@ moe_status_t moe_workspace_size(const moe_ctx* ctx, size_t* bytes) {
   return MOE_OK;
 }
 
-moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, void* stream) {
+// Arguments of the layout step; checks the routing pointer.
+static moe_status_t plan_args(moe_ctx* ctx, const int32_t* topk_ids, void* ws, moe::PlanArgs* out) {
   moe_status_t st = check_ws(ctx, ws);
   if (st != MOE_OK) return st;
   const moe_shape_t& s = ctx->shape;
   const int64_t A = s.T * s.topk;
   if (A > 0 && !topk_ids) return MOE_ERR_INVALID_ARG;
   if (topk_ids && !aligned16(topk_ids)) return MOE_ERR_MISALIGNED;
-  moe::PlanArgs p;
+  moe::PlanArgs& p = *out;
   memset(&p, 0, sizeof(p));
   p.topk_ids = topk_ids;
   p.A = A;
@@ -433,19 +434,20 @@ moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, vo
   p.chunk_hist = at<int32_t>(ws, ctx->ws.chunk_hist);
   p.chunk_rank = at<int32_t>(ws, ctx->ws.chunk_rank);
   if (ctx->ws.partial_rows > 0) p.block_vrow = at<int32_t>(ws, ctx->ws.block_vrow);
-  return cuda_status(moe::launch_plan(p, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
 }
 
-// topk_ids: given by moe_forward, whose small problems then quantise with
-// destinations formed from the routing, beside the plan (launch_quant_scatter).
-static moe_status_t quant_scatter(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids, void* ws,
-                                  void* stream) {
+// Arguments of the quant-scatter step; checks the activation pointer.
+// topk_ids (moe_forward's small problems): destinations formed from the
+// routing instead of read from src2dst.
+static moe_status_t quant_args(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids, void* ws,
+                               moe::QuantArgs* out) {
   moe_status_t st = check_ws(ctx, ws);
   if (st != MOE_OK) return st;
   const moe_shape_t& s = ctx->shape;
   if (s.T > 0 && !x_bf16) return MOE_ERR_INVALID_ARG;
   if (x_bf16 && !aligned16(x_bf16)) return MOE_ERR_MISALIGNED;
-  moe::QuantArgs q;
+  moe::QuantArgs& q = *out;
   memset(&q, 0, sizeof(q));
   q.x = x_bf16;
   q.src2dst = at<int32_t>(ws, ctx->ws.src2dst);
@@ -463,11 +465,21 @@ static moe_status_t quant_scatter(moe_ctx* ctx, const void* x_bf16, const int32_
   q.E_global = s.E_global;
   q.E_local = s.E_local;
   q.expert_start = s.expert_start;
-  return cuda_status(moe::launch_quant_scatter(q, static_cast<cudaStream_t>(stream)));
+  return MOE_OK;
+}
+
+moe_status_t moe_plan_layout(moe_ctx* ctx, const int32_t* topk_ids, void* ws, void* stream) {
+  moe::PlanArgs p;
+  const moe_status_t st = plan_args(ctx, topk_ids, ws, &p);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_plan(p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_quant_scatter(moe_ctx* ctx, const void* x_bf16, void* ws, void* stream) {
-  return quant_scatter(ctx, x_bf16, nullptr, ws, stream);
+  moe::QuantArgs q;
+  const moe_status_t st = quant_args(ctx, x_bf16, nullptr, ws, &q);
+  if (st != MOE_OK) return st;
+  return cuda_status(moe::launch_quant_scatter(q, static_cast<cudaStream_t>(stream)));
 }
 
 static moe_status_t run_gemm(moe_ctx* ctx, void* ws, void* stream, int stage) {
@@ -525,8 +537,19 @@ moe_status_t moe_combine(moe_ctx* ctx, const float* topk_weights, const void* ws
 moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
                          void* ws, void* out_bf16, void* stream) {
   moe_status_t st;
-  if ((st = moe_plan_layout(ctx, topk_ids, ws, stream)) != MOE_OK) return st;
-  if ((st = quant_scatter(ctx, x_bf16, topk_ids, ws, stream)) != MOE_OK) return st;
+  if (ctx && moe::plan_is_small(ctx->shape.T * ctx->shape.topk, ctx->shape.E_local)) {
+    // small problems: the plan and the quant-scatter in one launch, the
+    // quantising CTAs forming their tokens' destinations from the routing
+    moe::PlanArgs p;
+    moe::QuantArgs q;
+    if ((st = plan_args(ctx, topk_ids, ws, &p)) != MOE_OK) return st;
+    if ((st = quant_args(ctx, x_bf16, topk_ids, ws, &q)) != MOE_OK) return st;
+    if ((st = cuda_status(moe::launch_plan_quant_small(p, q, static_cast<cudaStream_t>(stream)))) != MOE_OK)
+      return st;
+  } else {
+    if ((st = moe_plan_layout(ctx, topk_ids, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_quant_scatter(ctx, x_bf16, ws, stream)) != MOE_OK) return st;
+  }
   if ((st = moe_grouped_gemm_w13_act(ctx, ws, stream)) != MOE_OK) return st;
   if ((st = moe_grouped_gemm_w2(ctx, ws, stream)) != MOE_OK) return st;
   return moe_combine(ctx, topk_weights, ws, out_bf16, stream);
@@ -535,8 +558,11 @@ moe_status_t moe_forward(moe_ctx* ctx, const void* x_bf16, const int32_t* topk_i
 int32_t moe_forward_launches(const moe_ctx* ctx) {
   if (!ctx) return -1;
   const moe_shape_t& s = ctx->shape;
-  int n = moe::plan_launch_count(s.T * s.topk, s.E_local);   // plan
-  if (s.T > 0) n += 2;                          // quant + combine
+  int n;
+  if (moe::plan_is_small(s.T * s.topk, s.E_local))
+    n = 1 + (s.T > 0 ? 1 : 0);                  // plan + quant in one launch, combine
+  else
+    n = moe::plan_launch_count(s.T * s.topk, s.E_local) + (s.T > 0 ? 2 : 0);   // plan, quant + combine
   if (ctx->ws.blocks > 0) {
     n += 2;                                     // two GEMMs
     n += (ctx->ws.k_splits1 > 1) + (ctx->ws.k_splits2 > 1);   // their split-K reductions

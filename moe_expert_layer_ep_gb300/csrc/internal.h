@@ -158,6 +158,9 @@ inline bool plan_is_small(int64_t A, int32_t E_local) { return A <= kPlanSmallMa
 cudaError_t launch_plan(const PlanArgs& p, cudaStream_t s);
 int plan_launch_count(int64_t A, int32_t E_local);   // kernels one launch_plan enqueues
 cudaError_t launch_quant_scatter(const QuantArgs& q, cudaStream_t s);
+// moe_forward's first step for small problems (plan_is_small, with q.topk_ids
+// set): the one-CTA plan and the quant-scatter in one launch.
+cudaError_t launch_plan_quant_small(const PlanArgs& p, const QuantArgs& q, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& c, cudaStream_t s);
 // Tensor maps of one grouped-GEMM launch.
 struct GemmMaps {

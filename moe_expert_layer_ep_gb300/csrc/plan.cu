@@ -19,6 +19,7 @@
 //   3. plan_finalize    src2dst = start + chunk offset + rank; m_indices.
 #include "common.cuh"
 #include "internal.h"
+#include "quant_row.cuh"
 
 namespace moe {
 
@@ -267,14 +268,14 @@ __global__ void __launch_bounds__(256) plan_finalize(PlanArgs p) {
 // in earlier lanes of its warp (warp match), as in the three-kernel path, so
 // the outputs are identical to it.
 
-__global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
+// Called by all 1024 threads of one CTA, after the kernel's wait for its
+// predecessor.
+__device__ void plan_small_body(const PlanArgs& p) {
   __shared__ int s_wcnt[32 * kPlanSmallMaxE];   // [warp][expert] counts of the current chunk
   __shared__ int s_tab[3 * kPlanSmallMaxE];     // start, padded, counts (the running per-expert counts)
   __shared__ int s_warp[32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E_local;
-  pdl_wait();
-  pdl_trigger();
   // the status word reports the first data error of this pass
   if (p.clear_status && tid < 4) p.status[tid] = 0;
   __syncthreads();
@@ -333,8 +334,69 @@ __global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
   if (!p.masked) fill_m_indices(p, s_tab, tid, 1024);
 }
 
+__global__ void __launch_bounds__(1024) plan_small(PlanArgs p) {
+  pdl_wait();
+  pdl_trigger();
+  plan_small_body(p);
+}
+
+// The first step of moe_forward for small problems, in one launch: CTA 0
+// plans the layout (plan_small_body) while every other CTA quantises four
+// tokens, one per 256 threads, into destination rows it forms itself from
+// the routing by the plan's rule (quant_row.cuh), so neither waits for the
+// other.  The kernels after it see both complete.
+constexpr int kPqTokens = 1024 / kQuantThreads;   // tokens per quantising CTA
+
+template <bool kFP8, bool kMX>
+__global__ void __launch_bounds__(1024) plan_quant_small_kernel(PlanArgs p, QuantArgs q) {
+  __shared__ int16_t s_lid[kPlanSmallMaxA];
+  __shared__ int s_cnt[kPlanSmallMaxE];
+  __shared__ int64_t s_dst[kPqTokens][kMaxTopk];
+  __shared__ int64_t s_blk[kPqTokens][kMaxTopk];
+  __shared__ int s_row[kPqTokens][kMaxTopk];
+  __shared__ int s_any[kPqTokens];
+  pdl_wait();     // routing and activations come from earlier kernels
+  pdl_trigger();
+  if (blockIdx.x == 0) {
+    plan_small_body(p);
+    return;
+  }
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int x = tid; x < q.E_local; x += 1024) s_cnt[x] = 0;
+  if (tid < kPqTokens) s_any[tid] = 0;
+  __syncthreads();
+  fill_routing(q, s_lid, s_cnt, tid, 1024);
+  __syncthreads();
+  // warp w: token w / 8 of this CTA, selections j = w % 8, w % 8 + 8, ...
+  const int g = warp >> 3;
+  const int64_t t = static_cast<int64_t>(blockIdx.x - 1) * kPqTokens + g;
+  if (t < q.T) {
+    for (int j = warp & 7; j < q.topk; j += 8) {
+      const int64_t d = token_destination(q, s_lid, s_cnt, t, j, lane);
+      if (lane == 0) {
+        s_dst[g][j] = d;
+        if (d >= 0) {
+          s_any[g] = 1;
+          dest_block(q, d, &s_blk[g][j], &s_row[g][j]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (t < q.T && s_any[g]) quant_scatter_row<kFP8, kMX>(q, t, s_dst[g], s_blk[g], s_row[g], tid & (kQuantThreads - 1));
+}
+
 }  // namespace
 
+
+cudaError_t launch_plan_quant_small(const PlanArgs& p, const QuantArgs& q, cudaStream_t s) {
+  PlanArgs pc = p;
+  pc.clear_status = 1;   // the planning CTA clears the status word; nothing else here sets it
+  const dim3 grid(static_cast<unsigned>(1 + (q.T + kPqTokens - 1) / kPqTokens)), block(1024);
+  if (q.mx) return launch_pdl(plan_quant_small_kernel<true, true>, grid, block, 0, s, pc, q);
+  if (q.fp8) return launch_pdl(plan_quant_small_kernel<true, false>, grid, block, 0, s, pc, q);
+  return launch_pdl(plan_quant_small_kernel<false, false>, grid, block, 0, s, pc, q);
+}
 
 int plan_launch_count(int64_t A, int32_t E_local) {
   if (plan_is_small(A, E_local)) return 1;

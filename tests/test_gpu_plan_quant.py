@@ -120,10 +120,11 @@ SMALL_FORWARD_CASES = [c for c in CASES if 0 < c["T"] * c["topk"] <= 2048 and c[
 
 @pytest.mark.parametrize("case", SMALL_FORWARD_CASES, ids=[_ids(c) for c in SMALL_FORWARD_CASES])
 def test_forward_quant_destinations_match_the_plan(case):
-    """Inside moe_forward, small problems quantise with destination rows the
-    quant kernel forms from the routing itself (beside the plan, not after
-    it).  Its expert rows and scales must be the bytes the plan-driven
-    moe_quant_scatter writes, and its src2dst the plan's."""
+    """Inside moe_forward, small problems plan and quantise in one launch,
+    the quantising CTAs forming their destination rows from the routing
+    (beside the planning CTA, not after it).  The expert rows and scales
+    must be the bytes the plan-driven moe_quant_scatter writes, and src2dst
+    the plan's."""
     p = Problem(**case, weight_device="cpu")
     ref = p.gpu()
     ref.plan()
