@@ -190,38 +190,38 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       for (int64_t i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const RtItem it = rt_item(r, i);
         for (int seg = it.seg0; seg < it.seg1 && ok; ++seg, ++iter) {
-        const int acc = iter & 1;
-        if (!mbar_wait_bounded(&tempty[acc], ((iter >> 1) & 1) ^ 1, abort_flag, r.timeout_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kRtTileN);
-        int kb0, nkb;
-        seg_blocks(r, seg, &kb0, &nkb);
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort_flag, r.timeout_ns)) {
+          const int acc = iter & 1;
+          if (!mbar_wait_bounded(&tempty[acc], ((iter >> 1) & 1) ^ 1, abort_flag, r.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t a_desc = smem_desc(smem_u32(smem + kRtOffA + stage * kRtABytes), 16, 1024, kSwizzle128B);
-          const uint32_t b_addr = smem_u32(smem + kRtOffB + stage * kRtBBytes);
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(acc * kRtTileN);
+          int kb0, nkb;
+          seg_blocks(r, seg, &kb0, &nkb);
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!mbar_wait_bounded(&full[stage], phase, abort_flag, r.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t a_desc = smem_desc(smem_u32(smem + kRtOffA + stage * kRtABytes), 16, 1024, kSwizzle128B);
+            const uint32_t b_addr = smem_u32(smem + kRtOffB + stage * kRtBBytes);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int p = 0; p < kRtPlanes; ++p)
-              mma_bf16(d_tmem, a_desc + 2 * k,
-                       smem_desc(b_addr + p * kRtBPlaneBytes, 16, 1024, kSwizzle128B) + 2 * k, kRtIdesc,
-                       (kb | k | p) != 0);
-          tc_commit(&empty[stage]);
-          if (++stage == kRtStages) {
-            stage = 0;
-            phase ^= 1;
+              for (int p = 0; p < kRtPlanes; ++p)
+                mma_bf16(d_tmem, a_desc + 2 * k,
+                         smem_desc(b_addr + p * kRtBPlaneBytes, 16, 1024, kSwizzle128B) + 2 * k, kRtIdesc,
+                         (kb | k | p) != 0);
+            tc_commit(&empty[stage]);
+            if (++stage == kRtStages) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-        }
-        if (!ok) break;
-        tc_commit(&tfull[acc]);
+          if (!ok) break;
+          tc_commit(&tfull[acc]);
         }
       }
       if (!ok) {
